@@ -1,0 +1,222 @@
+/*
+ * tsd.h -- C ABI of the GB300 tree-speculative-decoding verify step.
+ *
+ * One verify step of tree-structured speculative decoding, as four calls on
+ * one CUDA stream:
+ *
+ *   tsd_tree_build        per-position top-k of the draft marginals, then the
+ *                         greedy best-first draft tree under a node budget D
+ *   tsd_tree_verify_attn  branch-aware attention of every tree node over the
+ *                         shared prefix KV cache plus its own ancestors
+ *   tsd_accept_walk       target argmax per node, greedy walk to the accepted
+ *                         path, bonus (correction) token, chain id
+ *   tsd_commit_path       copy the accepted path's scratch KV into the cache
+ *
+ * Sources of the operations (web pages, by title and section):
+ *   "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4 for
+ *    Efficient Inference" (review): Key idea (tree under a verification
+ *    budget D); Background, research gap item 1 (a candidate sees only its own
+ *    ancestors); "How it works" toy example steps 1-6 (top-k expansion, budget
+ *    pruning, tree attention fed with layout and metadata only, chains, greedy
+ *    accepted path, commit of that path only); "Secret weapon" (scratch pad).
+ *   "Cost-Aware Diffusion Draft Trees for Speculative Decoding": Method items
+ *    1-2 (per-position marginals of a one-pass drafter; the greedy best-first
+ *    tree picks the node of highest prefix probability).
+ *   "DSpark: Speculative decoding ...": Architecture, decoding cycle (anchor
+ *    token, accepted prefix, rejected draft, correction token).
+ *
+ * Conventions shared by every call
+ *   - All array pointers are DEVICE pointers, allocated and owned by the
+ *     caller, 16-byte aligned, dense row-major in the layouts given below.
+ *     The library never allocates, frees or synchronises; scratch memory is a
+ *     caller-provided workspace of the size the matching *_workspace_size call
+ *     returns (for the current device).
+ *   - Every call only enqueues kernels on `stream` and returns.  Outputs are
+ *     valid once the stream has reached that point.
+ *   - The return value reports HOST-side validation and launch errors.  On any
+ *     non-OK return nothing was enqueued, except TSD_ERR_CUDA from a failed
+ *     launch (check cudaGetLastError semantics).
+ *   - Problems found on the device (a request that would overflow the cache,
+ *     a malformed caller-supplied tree) are written to the caller's `err`
+ *     word: 0 means OK, otherwise (TSD_DEV_ERR_* code) | request index.  The
+ *     first error wins; the library never clears `err` (the caller zeroes it).
+ *     The offending request is skipped; the others are processed normally.
+ *   - Row 0 of every tree is the root (the anchor token produced by the target
+ *     in the previous round); rows 1..D are draft nodes; R = 1 + D.
+ *   - Limits: 1 <= k <= 32, k <= V, 1 <= S <= 16, 1 <= D <= 64 and
+ *     D <= sum_{s=1..S} k^s; Hq % Hkv == 0; head dims as listed per call.
+ */
+#ifndef TSD_H_
+#define TSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream; ABI-identical to cudaStream_t (NULL = the legacy stream). */
+typedef struct CUstream_st* tsd_stream_t;
+
+typedef enum {
+  TSD_OK = 0,
+  TSD_ERR_INVALID_ARG = 1,    /* bad size, null or misaligned pointer, short workspace */
+  TSD_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+  TSD_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
+  TSD_ERR_DEVICE = 4,         /* reserved: device-side problems go to the err word */
+  TSD_ERR_DEVICE_TIMEOUT = 5  /* a bounded device wait gave up */
+} tsd_status;
+
+/* Codes in the device error word (high byte); low 24 bits = request index. */
+#define TSD_DEV_ERR_CAPACITY 0x01000000 /* commit would pass the cache capacity */
+#define TSD_DEV_ERR_BAD_TREE 0x02000000 /* parent/row out of range, walk deeper than S */
+#define TSD_DEV_ERR_TIMEOUT  0x03000000 /* a bounded wait inside a kernel gave up */
+#define TSD_DEV_ERR_MASK     0x7f000000
+
+/* Element types of attention operands. */
+#define TSD_F32 0
+#define TSD_BF16 1
+
+/* Static text for a status code. */
+const char* tsd_status_string(tsd_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int tsd_version(void);
+
+/* --------------------------------------------------------------------------
+ * tsd_tree_build
+ *
+ * Per-position top-k then greedy best-first tree ("Cost-Aware Diffusion Draft
+ * Trees", Method 2; V4 review, toy steps 1-2).
+ *
+ * probs     [B][S][V] fp32: the draft's per-position marginal distributions
+ *           (non-negative, no NaN; -0.0 counts as +0.0).
+ * root_tok  [B] int32: the root (anchor) token of each request.
+ * Outputs, all [B][1+D]:
+ *   token   int32  row's token (row 0 = root_tok)
+ *   parent  int32  parent row (-1 for the root)
+ *   depth   int32  0 for the root, else 1..S
+ *   score   fp32   prefix probability: fp32 product of the top-k
+ *                  probabilities along the path, in depth order (1.0 for root)
+ *   mask    uint64 bit j-1 set iff row j (j >= 1) is an ancestor of the row or
+ *                  the row itself; the root is implicit (visible to all rows)
+ *   is_leaf uint8  1 iff no row has this row as parent
+ *
+ * Children of a node at depth d are the k most probable tokens of position
+ * d+1, ordered by (probability desc, token id asc).  Rows 1..D are the first D
+ * paths in the total order (score desc, depth asc, tuple of top-k ranks
+ * lexicographic asc), which lists parents before children.
+ * ws: tsd_tree_build_workspace_size(B, S, V, k) bytes of device scratch.
+ * -------------------------------------------------------------------------- */
+size_t tsd_tree_build_workspace_size(int B, int S, int V, int k);
+
+tsd_status tsd_tree_build(const float* probs, int B, int S, int V, int k, int D,
+                          const int32_t* root_tok, int32_t* token,
+                          int32_t* parent, int32_t* depth, float* score,
+                          uint64_t* mask, uint8_t* is_leaf, void* ws,
+                          size_t ws_bytes, int32_t* err, tsd_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * tsd_tree_verify_attn
+ *
+ * Branch-aware tree attention (V4 review, research gap item 1 and toy step 3).
+ * For request b, tree row r and query head h (KV head h / (Hq/Hkv)), the
+ * visible keys are the cached prefix positions 0..prefix_len[b]-1, the root
+ * row of the scratch pad, and every scratch row j >= 1 with bit j-1 of
+ * mask[b][r] set (for r = 0: the root only).  Output is
+ *   out = softmax(scale * q . K^T) V,   lse = natural log of the softmax
+ *   denominator including its max (logsumexp of the scaled scores),
+ * accumulated in fp32; out has the element type of q.
+ *
+ * Layouts (element type `dtype`, TSD_F32 or TSD_BF16):
+ *   q      [B][R][Hq][dk]
+ *   kcache [B][Hkv][cap][dk]      vcache [B][Hkv][cap][dv]
+ *   ktree  [B][R][Hkv][dk]        vtree  [B][R][Hkv][dv]   (scratch pad)
+ *   prefix_len [B] int32 (0 <= P_b <= cap; values outside are clamped)
+ *   mask   [B][R] uint64 (as produced by tsd_tree_build)
+ *   out    [B][R][Hq][dv]         lse [B][R][Hq] fp32
+ * With v_aliases_k (latent attention) the value is the first dv entries of
+ * the key; vcache/vtree are ignored and may be NULL; dv <= dk.
+ * Supported head dims: dk == dv in {64, 128}, or dk = 576, dv = 512 with
+ * v_aliases_k.  fp32 inputs are computed on CUDA cores in fp32 (never TF32).
+ * ws: tsd_verify_workspace_size(desc) bytes (0 is a valid size).
+ * -------------------------------------------------------------------------- */
+typedef struct {
+  int B;            /* requests */
+  int R;            /* tree rows per request, 1 + D, 1 <= R <= 65 */
+  int Hq, Hkv;      /* query heads, KV heads (Hq % Hkv == 0) */
+  int dk, dv;       /* key/query and value head dims */
+  int cap;          /* cache capacity in tokens (positions per head) */
+  int dtype;        /* TSD_F32 or TSD_BF16 */
+  int v_aliases_k;  /* 1: value = key[:dv] (latent KV), 0: separate V */
+  float scale;      /* softmax scale applied to q . k */
+} tsd_attn_desc;
+
+size_t tsd_verify_workspace_size(const tsd_attn_desc* desc);
+
+tsd_status tsd_tree_verify_attn(const tsd_attn_desc* desc, const void* q,
+                                const void* kcache, const void* vcache,
+                                const int32_t* prefix_len, const void* ktree,
+                                const void* vtree, const uint64_t* mask,
+                                void* out, float* lse, void* ws,
+                                size_t ws_bytes, int32_t* err,
+                                tsd_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * tsd_accept_walk
+ *
+ * Greedy accepted-path selection (V4 review, toy steps 5-6; DSpark decoding
+ * cycle).  tgt[r] = argmax_v logits[b][r][v] (ties to the lowest v).  Starting
+ * at the root u = 0: while some child c of u (parent[c] == u) has token[c] ==
+ * tgt[u], append the lowest such c and move to it.
+ *
+ * logits     [B][1+D][V] fp32 target logits of every tree row (no NaN).
+ * token/parent [B][1+D] int32, mask [B][1+D] uint64, is_leaf [B][1+D] uint8:
+ *            a tree as produced by tsd_tree_build (or any tree with parent[c]
+ *            < c, depth <= S; a violation sets TSD_DEV_ERR_BAD_TREE).
+ * Outputs:
+ *   tgt          [B][1+D] int32, optional (NULL to skip): the argmax per row
+ *   accept_len   [B] int32: L, the number of accepted draft rows
+ *   accept_rows  [B][S+1] int32: 0, then the L accepted rows, then -1
+ *   bonus        [B] int32: tgt at the last accepted row (next round's root)
+ *   chain_id     [B] int32: lowest leaf row whose ancestor-or-self set holds
+ *                the last accepted row (the chain of the tree's decomposition
+ *                into root-to-leaf chains); -1 when L = 0
+ * ws: tsd_accept_walk_workspace_size(B, D, V) bytes.
+ * -------------------------------------------------------------------------- */
+size_t tsd_accept_walk_workspace_size(int B, int D, int V);
+
+tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, int V,
+                           const int32_t* token, const int32_t* parent,
+                           const uint64_t* mask, const uint8_t* is_leaf,
+                           int32_t* tgt, int32_t* accept_len,
+                           int32_t* accept_rows, int32_t* bonus,
+                           int32_t* chain_id, void* ws, size_t ws_bytes,
+                           int32_t* err, tsd_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * tsd_commit_path
+ *
+ * Accepted-path commit (V4 review, "Secret weapon" and toy step 6): only the
+ * accepted chain's KV leaves the scratch pad.  For each request b with
+ * P = prefix_len[b] and L = accept_len[b]: scratch rows accept_rows[b][0..L]
+ * are copied, in order, to cache positions P..P+L of every KV head (K, and V
+ * unless desc->v_aliases_k), then prefix_len[b] = P + 1 + L.  Rejected rows
+ * and all other cache positions are left untouched.  A request with
+ * P + 1 + L > cap is skipped and reported as TSD_DEV_ERR_CAPACITY; a row
+ * index outside [0, R) as TSD_DEV_ERR_BAD_TREE.
+ * desc gives B, R, Hkv, dk, dv, cap, dtype, v_aliases_k (Hq, scale unused).
+ * S is the accept_rows row length minus one.  No workspace.
+ * -------------------------------------------------------------------------- */
+tsd_status tsd_commit_path(const tsd_attn_desc* desc, int S, const void* ktree,
+                           const void* vtree, const int32_t* accept_rows,
+                           const int32_t* accept_len, void* kcache,
+                           void* vcache, int32_t* prefix_len, int32_t* err,
+                           tsd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSD_H_ */

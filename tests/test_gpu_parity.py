@@ -1,0 +1,430 @@
+"""GPU parity of every call of the C ABI against the CPU oracle.
+
+Trees, argmax, walks and committed caches must match bit for bit; attention
+must match within 1e-5 max abs (fp32) or 2e-2 max abs (bf16, fp32 accumulate).
+Full-size workloads are checked on sampled attention rows the oracle computes
+one by one; reduced sizes (several tiles plus a ragged tail) on every row.
+"""
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.conftest import load_golden
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import tree_speculative_decoding_tsd_gb300 as T
+    from tree_speculative_decoding_tsd_gb300 import workloads as W
+    from tree_speculative_decoding_tsd_gb300.step import TreeVerifyStep
+else:  # collected on CPU only to be deselected
+    from tree_speculative_decoding_tsd_gb300 import workloads as W
+
+DEV = "cuda:0"
+NAMES = ["toy", "qwen", "batched", "long", "mla"]
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+
+
+def _tol(w):
+    return TOL[w.dtype]
+
+
+@functools.lru_cache(maxsize=16)
+def inputs(name, **over):
+    """CPU inputs of a workload plus the oracle's tree (cached)."""
+    w = W.WORKLOADS[name]
+    if over:
+        w = w.scaled(**dict(over))
+    lg = W.draft_logits(w)
+    probs = W.draft_probs(w, lg)
+    root = W.root_tokens(w)
+    tp, ti = oracle.topk(probs.numpy(), w.k)
+    tree = oracle.tree(tp, ti, w.D, root.numpy(), method="beam")
+    return dict(w=w, logits=lg, probs=probs, root=root, tp=tp, ti=ti, tree=tree)
+
+
+def attn_inputs(w):
+    q = W.queries(w)
+    kc, vc = W.kv_cache(w)
+    kt, vt = W.tree_kv(w)
+    return q, kc, vc, W.prefix_lens(w), kt, vt
+
+
+def gpu(*ts):
+    return [None if t is None else t.to(DEV) for t in ts]
+
+
+def run_tree(step, probs, root):
+    p, r = gpu(probs, root)
+    step.build(p, r)
+    torch.cuda.synchronize()
+    t = step.tree
+    return dict(token=t.token.cpu().numpy(), parent=t.parent.cpu().numpy(),
+                depth=t.depth.cpu().numpy(), score=t.score.cpu().numpy(),
+                mask=t.mask.cpu().numpy().view(np.uint64), is_leaf=t.is_leaf.cpu().numpy())
+
+
+def assert_tree_equal(got, ref):
+    for key in ("token", "parent", "depth", "is_leaf"):
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+    np.testing.assert_array_equal(got["score"].view(np.uint32), ref["score"].view(np.uint32))
+    np.testing.assert_array_equal(got["mask"], ref["mask"])
+
+
+def set_tree(step, tree):
+    t = step.tree
+    t.token.copy_(torch.from_numpy(tree["token"]))
+    t.parent.copy_(torch.from_numpy(tree["parent"]))
+    t.depth.copy_(torch.from_numpy(tree["depth"]))
+    t.score.copy_(torch.from_numpy(tree["score"]))
+    t.mask.copy_(torch.from_numpy(tree["mask"].view(np.int64)))
+    t.is_leaf.copy_(torch.from_numpy(tree["is_leaf"]))
+
+
+# --------------------------------------------------------------- smoke --
+
+def test_smoke():
+    import __graft_entry__
+    __graft_entry__.smoke()
+
+
+# ---------------------------------------------------------- tree build --
+
+@pytest.mark.parametrize("name", NAMES)
+def test_tree_build_full_size(name):
+    d = inputs(name)
+    w = d["w"]
+    step = TreeVerifyStep.for_workload(w, DEV)
+    got = run_tree(step, d["probs"], d["root"])
+    assert_tree_equal(got, d["tree"])
+    assert int(step.err[0]) == 0
+
+
+@pytest.mark.parametrize("B,S,V,k,D,quant", [
+    (3, 3, 1001, 3, 12, None),      # rows not 16-byte aligned
+    (2, 5, 4099, 1, 5, None),       # chain (linear speculation)
+    (2, 2, 3000, 32, 64, None),     # k = 32, D = 64
+    (1, 16, 700, 2, 64, None),      # deepest tree
+    (4, 4, 2053, 8, 40, 256),       # heavy ties in the marginals
+    (2, 3, 32, 32, 40, 16),         # V == k: every token kept, ties
+    (3, 2, 200000, 4, 9, None),     # long rows over many chunks
+])
+def test_tree_build_edge_cases(B, S, V, k, D, quant):
+    g = torch.Generator().manual_seed(B * 1000 + S * 100 + k)
+    x = torch.randn((B, S, V), generator=g, dtype=torch.float64) * 2.0
+    p = torch.softmax(x, -1)
+    if quant:
+        p = torch.round(p * quant) / quant
+    probs = p.float().contiguous()
+    root = torch.randint(0, V, (B,), generator=g).int()
+    tp, ti = oracle.topk(probs.numpy(), k)
+    ref = oracle.tree(tp, ti, D, root.numpy(), method="beam")
+    step = TreeVerifyStep(B, S, V, k, D, 2, 1, 64, 64, 8, torch.float32, False, 0.125, DEV)
+    assert_tree_equal(run_tree(step, probs, root), ref)
+
+
+def test_tree_build_toy_fixture():
+    g = load_golden("toy_tree.txt")
+    probs = torch.tensor([[g["p1"], g["p2"]]], dtype=torch.float32)
+    step = TreeVerifyStep(1, 2, 3, 2, 3, 1, 1, 64, 64, 8, torch.float32, False, 0.125, DEV)
+    got = run_tree(step, probs, torch.tensor(g["root"], dtype=torch.int32))
+    for key in ("token", "parent", "depth", "is_leaf"):
+        assert list(got[key][0]) == g[key], key
+    assert list(got["mask"][0]) == g["mask"]
+
+
+# ----------------------------------------------------------- attention --
+
+def check_attention(w, q, kc, vc, plen, kt, vt, mask, sel=None):
+    step = TreeVerifyStep.for_workload(w, DEV)
+    step.tree.mask.copy_(torch.from_numpy(np.ascontiguousarray(mask).view(np.int64)))
+    step.verify(*gpu(q, kc, vc, plen, kt, vt))
+    torch.cuda.synchronize()
+    out = step.out.float().cpu().numpy().astype(np.float64)
+    lse = step.lse.cpu().numpy().astype(np.float64)
+    ref_out, ref_lse = oracle.verify_attn(W.bits(q), W.bits(kc), None if vc is None else W.bits(vc),
+                                          plen.numpy(), W.bits(kt),
+                                          None if vt is None else W.bits(vt), mask, w.scale,
+                                          v_aliases_k=w.v_aliases_k, dv=w.dv, sel=sel)
+    if sel is not None:
+        out = np.stack([out[b, r, h] for b, r, h in sel])
+        lse = np.array([lse[b, r, h] for b, r, h in sel])
+    err = np.abs(out - ref_out).max()
+    assert err <= _tol(w), f"max abs err {err}"
+    assert np.abs(lse - ref_lse).max() <= _tol(w) * 5e-2 + 1e-5
+    return step
+
+
+def sample_rows(w, n, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = {(0, 0, 0), (w.B - 1, w.R - 1, w.Hq - 1), (0, w.R - 1, w.Hq // 2), (w.B - 1, 1, 0)}
+    while len(rows) < n:
+        rows.add((int(rng.integers(w.B)), int(rng.integers(w.R)), int(rng.integers(w.Hq))))
+    return np.array(sorted(rows), np.int32)
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_verify_attention_full_size_sampled(name):
+    d = inputs(name)
+    w = d["w"]
+    check_attention(w, *attn_inputs(w), d["tree"]["mask"], sel=sample_rows(w, 40))
+
+
+REDUCED = {
+    # all rows checked; prefixes span several KV tiles/splits and a ragged tail
+    "toy": dict(),
+    "qwen": dict(P=777, P_min=777),
+    "batched": dict(B=5, P=1100, P_min=0, V=5000),
+    "long": dict(B=2, P=1500, P_min=1500, V=3000),
+    "mla": dict(B=2, P=300, P_min=300, V=2000),
+    "qwen_f32": dict(dtype="f32", P=513, P_min=513),
+}
+
+
+@pytest.mark.parametrize("key", list(REDUCED))
+def test_verify_attention_reduced_all_rows(key):
+    name = key.split("_")[0]
+    d = inputs(name, **REDUCED[key])
+    w = d["w"]
+    check_attention(w, *attn_inputs(w), d["tree"]["mask"])
+
+
+def test_verify_attention_empty_and_tiny_prefixes():
+    w = W.WORKLOADS["qwen"].scaled(B=6, P=40, P_min=0, V=500)
+    d = inputs("qwen", B=6, P=40, P_min=0, V=500)
+    q, kc, vc, _, kt, vt = attn_inputs(w)
+    plen = torch.tensor([0, 1, 2, 39, 40, 17], dtype=torch.int32)
+    check_attention(w, q, kc, vc, plen, kt, vt, d["tree"]["mask"])
+
+
+def test_verify_branch_isolation_bit_exact():
+    """Changing scratch K/V of rows outside a node's ancestor path leaves the
+    node's output bit-identical (research gap item 1 of the V4 review)."""
+    d = inputs("qwen", P=300, P_min=300, V=4000)
+    w, tree = d["w"], d["tree"]
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    s0 = check_attention(w, q, kc, vc, plen, kt, vt, tree["mask"])
+    base = s0.out.clone()
+    par = tree["parent"][0]
+    j = int(w.R - 1)                        # perturb the last row (a leaf)
+    kt2, vt2 = kt.clone(), vt.clone()
+    kt2[0, j] += 1.0
+    vt2[0, j] -= 1.0
+    s1 = TreeVerifyStep.for_workload(w, DEV)
+    s1.tree.mask.copy_(torch.from_numpy(tree["mask"].view(np.int64)))
+    s1.verify(*gpu(q, kc, vc, plen, kt2, vt2))
+    torch.cuda.synchronize()
+    for r in range(w.R):
+        anc, x = set(), r
+        while x > 0:
+            anc.add(x)
+            x = par[x]
+        same = torch.equal(s1.out[0, r], base[0, r])
+        assert same == (j not in anc), r
+
+
+def test_verify_batch_invariance_and_determinism():
+    d = inputs("batched", B=4, P=900, P_min=100, V=3000)
+    w, tree = d["w"], d["tree"]
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    full = check_attention(w, q, kc, vc, plen, kt, vt, tree["mask"])
+    again = TreeVerifyStep.for_workload(w, DEV)
+    again.tree.mask.copy_(full.tree.mask)
+    again.verify(*gpu(q, kc, vc, plen, kt, vt))
+    torch.cuda.synchronize()
+    assert torch.equal(again.out, full.out) and torch.equal(again.lse, full.lse)
+    b = 2
+    w1 = w.scaled(B=1)
+    one = TreeVerifyStep.for_workload(w1, DEV)
+    one.tree.mask.copy_(full.tree.mask[b:b + 1])
+    one.verify(*gpu(q[b:b + 1].contiguous(), kc[b:b + 1].contiguous(), vc[b:b + 1].contiguous(),
+                    plen[b:b + 1].contiguous(), kt[b:b + 1].contiguous(),
+                    vt[b:b + 1].contiguous()))
+    torch.cuda.synchronize()
+    assert torch.equal(one.out[0], full.out[b]) and torch.equal(one.lse[0], full.lse[b])
+
+
+# ---------------------------------------------------------- accept walk --
+
+def run_walk(step, logits):
+    (lg,) = gpu(logits)
+    step.accept(lg)
+    torch.cuda.synchronize()
+    wk = step.walk
+    return dict(tgt=wk.tgt.cpu().numpy(), accept_len=wk.accept_len.cpu().numpy(),
+                accept_rows=wk.accept_rows.cpu().numpy(), bonus=wk.bonus.cpu().numpy(),
+                chain_id=wk.chain_id.cpu().numpy())
+
+
+def assert_walk_equal(got, ref, tgt):
+    np.testing.assert_array_equal(got["tgt"], tgt)
+    for key in ("accept_len", "accept_rows", "bonus", "chain_id"):
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_accept_walk_full_size(name):
+    d = inputs(name)
+    w, tree = d["w"], d["tree"]
+    tl = W.target_logits(w, torch.from_numpy(tree["depth"]), d["logits"])
+    tgt = oracle.argmax(tl.numpy())
+    ref = oracle.accept_walk(tgt, tree, w.S)
+    step = TreeVerifyStep.for_workload(w, DEV)
+    set_tree(step, tree)
+    assert_walk_equal(run_walk(step, tl), ref, tgt)
+    assert int(step.err[0]) == 0
+
+
+@pytest.mark.parametrize("V", [13, 1001, 4097, 150001])
+def test_accept_walk_unaligned_rows_and_ties(V):
+    d = inputs("qwen", V=V, P=8, P_min=8)
+    w, tree = d["w"], d["tree"]
+    g = torch.Generator().manual_seed(V)
+    # integer-valued logits: many exact ties, argmax must take the lowest id
+    tl = torch.randint(-4, 4, (w.B, w.R, w.V), generator=g).float()
+    tgt = oracle.argmax(tl.numpy())
+    ref = oracle.accept_walk(tgt, tree, w.S)
+    step = TreeVerifyStep.for_workload(w, DEV)
+    set_tree(step, tree)
+    assert_walk_equal(run_walk(step, tl), ref, tgt)
+
+
+def _golden_tree(g):
+    R = len(g["token"])
+    tree = dict(token=np.array([g["token"]], np.int32), parent=np.array([g["parent"]], np.int32),
+                depth=np.array([g["depth"]], np.int32),
+                score=np.array([g["score"]], np.float32),
+                mask=np.array([g["mask"]], np.uint64), is_leaf=np.array([g["is_leaf"]], np.uint8))
+    return tree, R
+
+
+@pytest.mark.parametrize("fixture", ["toy_tree.txt", "dspark_chain.txt"])
+def test_accept_walk_page_fixtures(fixture):
+    g = load_golden(fixture)
+    tree, R = _golden_tree(g)
+    V = g["V"][0]
+    tl = torch.full((1, R, V), -1.0)
+    for r, t in enumerate(g["tgt"]):
+        tl[0, r, t] = 1.0
+    step = TreeVerifyStep(1, g["S"][0], V, g["k"][0], R - 1, 1, 1, 64, 64, 8, torch.float32,
+                          False, 0.125, DEV)
+    set_tree(step, tree)
+    got = run_walk(step, tl)
+    assert got["accept_len"][0] == g["accept_len"][0]
+    assert list(got["accept_rows"][0]) == g["accept_rows"]
+    assert got["bonus"][0] == g["bonus"][0] and got["chain_id"][0] == g["chain_id"][0]
+
+
+def test_accept_walk_reports_malformed_tree():
+    d = inputs("toy")
+    w, tree = d["w"], dict(d["tree"])
+    tree["parent"] = tree["parent"].copy()
+    tree["parent"][0, 2] = 3                         # parent after child
+    step = TreeVerifyStep.for_workload(w, DEV)
+    set_tree(step, tree)
+    got = run_walk(step, torch.zeros((w.B, w.R, w.V)))
+    e = int(step.err[0])
+    assert e & T.TSD_DEV_ERR_MASK == T.TSD_DEV_ERR_BAD_TREE and e & 0xFFFFFF == 0
+    assert got["accept_len"][0] == 0 and got["chain_id"][0] == -1
+
+
+# -------------------------------------------------------------- commit --
+
+def run_commit_case(w, accept_rows, accept_len, plen, seed=7):
+    g = torch.Generator().manual_seed(seed)
+    shape_k = (w.B, w.Hkv, w.cap, w.dk)
+    kc = torch.randn(shape_k, generator=g).to(w.torch_dtype)           # canary contents
+    vc = None if w.v_aliases_k else torch.randn((w.B, w.Hkv, w.cap, w.dv), generator=g).to(
+        w.torch_dtype)
+    kt, vt = W.tree_kv(w)
+    kc_ref = W.bits(kc).copy()
+    vc_ref = None if vc is None else W.bits(vc).copy()
+    pl_ref = plen.numpy().copy()
+    skipped = oracle.commit(W.bits(kt), None if vt is None else W.bits(vt), accept_rows,
+                            accept_len, kc_ref, vc_ref, pl_ref, w.S, v_aliases_k=w.v_aliases_k)
+    step = TreeVerifyStep.for_workload(w, DEV)
+    step.walk.accept_rows.copy_(torch.from_numpy(accept_rows))
+    step.walk.accept_len.copy_(torch.from_numpy(accept_len))
+    gk, gv, gpl, gkt, gvt = gpu(kc, vc, plen, kt, vt)
+    step.commit(gkt, gvt, gk, gv, gpl)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(W.bits(gk.cpu()), kc_ref)
+    if vc is not None:
+        np.testing.assert_array_equal(W.bits(gv.cpu()), vc_ref)
+    np.testing.assert_array_equal(gpl.cpu().numpy(), pl_ref)
+    return skipped, int(step.err[0])
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_commit_full_size(name):
+    d = inputs(name)
+    w, tree = d["w"], d["tree"]
+    tl = W.target_logits(w, torch.from_numpy(tree["depth"]), d["logits"])
+    ref = oracle.accept_walk(oracle.argmax(tl.numpy()), tree, w.S)
+    skipped, err = run_commit_case(w, ref["accept_rows"], ref["accept_len"], W.prefix_lens(w))
+    assert skipped == 0 and err == 0
+
+
+def test_commit_deep_paths_and_capacity_overflow():
+    w = W.WORKLOADS["qwen"].scaled(B=4, P=64, P_min=64, V=64)
+    S = w.S
+    rng = np.random.default_rng(3)
+    rows = np.full((w.B, S + 1), -1, np.int32)
+    ln = np.array([S, 3, 0, S], np.int32)
+    for b in range(w.B):
+        rows[b, 0] = 0
+        rows[b, 1:ln[b] + 1] = rng.choice(np.arange(1, w.R), ln[b], replace=False)
+    plen = torch.tensor([w.cap - S - 1, 10, w.cap - 1, w.cap - S], dtype=torch.int32)
+    skipped, err = run_commit_case(w, rows, ln, plen)
+    assert skipped == 1                                   # request 3 does not fit
+    assert err & T.TSD_DEV_ERR_MASK == T.TSD_DEV_ERR_CAPACITY and err & 0xFFFFFF == 3
+
+
+# ------------------------------------------------------------ full step --
+
+@pytest.mark.parametrize("name,over", [("toy", {}), ("qwen", {}),
+                                       ("batched", dict(B=6, V=20000)),
+                                       ("mla", dict(B=3, P=700, P_min=700, V=9000)),
+                                       ("long", dict(B=2, P=2000, P_min=2000, V=7000))])
+def test_full_step_chained(name, over):
+    d = inputs(name, **over)
+    w, tree = d["w"], d["tree"]
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    tl = W.target_logits(w, torch.from_numpy(tree["depth"]), d["logits"])
+    tgt = oracle.argmax(tl.numpy())
+    ref_walk = oracle.accept_walk(tgt, tree, w.S)
+    sel = sample_rows(w, 24, seed=5)
+    ref_out, _ = oracle.verify_attn(W.bits(q), W.bits(kc), None if vc is None else W.bits(vc),
+                                    plen.numpy(), W.bits(kt), None if vt is None else W.bits(vt),
+                                    tree["mask"], w.scale, v_aliases_k=w.v_aliases_k, dv=w.dv,
+                                    sel=sel)
+    kc_ref = W.bits(kc).copy()
+    vc_ref = None if vc is None else W.bits(vc).copy()
+    pl_ref = plen.numpy().copy()
+    oracle.commit(W.bits(kt), None if vt is None else W.bits(vt), ref_walk["accept_rows"],
+                  ref_walk["accept_len"], kc_ref, vc_ref, pl_ref, w.S, v_aliases_k=w.v_aliases_k)
+
+    step = TreeVerifyStep.for_workload(w, DEV)
+    g = gpu(d["probs"], d["root"], q, kc, vc, plen, kt, vt, tl)
+    step.run(*g)
+    torch.cuda.synchronize()
+    got_tree = dict(token=step.tree.token.cpu().numpy(), parent=step.tree.parent.cpu().numpy(),
+                    depth=step.tree.depth.cpu().numpy(), score=step.tree.score.cpu().numpy(),
+                    mask=step.tree.mask.cpu().numpy().view(np.uint64),
+                    is_leaf=step.tree.is_leaf.cpu().numpy())
+    assert_tree_equal(got_tree, tree)
+    out = step.out.float().cpu().numpy()
+    assert np.abs(np.stack([out[b, r, h] for b, r, h in sel]) - ref_out).max() <= _tol(w)
+    wk = step.walk
+    np.testing.assert_array_equal(wk.tgt.cpu().numpy(), tgt)
+    for key in ("accept_len", "accept_rows", "bonus", "chain_id"):
+        np.testing.assert_array_equal(getattr(wk, key).cpu().numpy(), ref_walk[key])
+    np.testing.assert_array_equal(W.bits(g[3].cpu()), kc_ref)
+    if vc is not None:
+        np.testing.assert_array_equal(W.bits(g[4].cpu()), vc_ref)
+    np.testing.assert_array_equal(g[5].cpu().numpy(), pl_ref)
+    assert int(step.err[0]) == 0

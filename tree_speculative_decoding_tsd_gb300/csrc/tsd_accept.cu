@@ -1,0 +1,142 @@
+// tsd_accept_walk: target argmax per tree row, then the greedy walk from the
+// root to the accepted path.
+//
+// Sources: "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4"
+// (review), "How it works" steps 4-6 (the tree splits into root-to-leaf
+// chains; the target checks all chains at once; the accepted prefix survives
+// where a linear chain would die; only the accepted chain is kept) and
+// "DSpark: Speculative decoding ...", Architecture, decoding cycle (drafts E
+// and F accepted, G rejected, the target's own token G* becomes the
+// correction / next anchor).
+//
+// K4 vocab_scan_kernel<true>: per-chunk argmax of every target-logit row
+//    (HBM-bound scan; ties go to the lowest id).
+// K5 accept_walk_kernel: one warp per request.  Merges the chunk maxima into
+//    tgt[r], checks the tree, walks: at row u, the child c (parent[c] == u)
+//    with token[c] == tgt[u] is accepted (lowest row if several), until no
+//    child matches.
+#include "tsd_common.cuh"
+#include "tsd_host.h"
+#include "tsd_scan.cuh"
+
+namespace tsd {
+namespace {
+
+constexpr int kMaxR = 65;
+
+__global__ void __launch_bounds__(32)
+accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
+                   const int32_t* __restrict__ token, const int32_t* __restrict__ parent,
+                   const uint64_t* __restrict__ mask, const uint8_t* __restrict__ is_leaf,
+                   int32_t* __restrict__ tgt_out, int32_t* __restrict__ accept_len,
+                   int32_t* __restrict__ accept_rows, int32_t* __restrict__ bonus,
+                   int32_t* __restrict__ chain_id, int32_t* __restrict__ err) {
+  __shared__ int32_t s_tgt[kMaxR], s_tok[kMaxR], s_par[kMaxR];
+  __shared__ uint64_t s_mask[kMaxR];
+  __shared__ uint8_t s_leaf[kMaxR];
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x;
+  const long o = (long)b * R;
+
+  bool bad = false;
+  for (int r = lane; r < R; r += 32) {
+    const uint64_t* src = part + (o + r) * nchunk;
+    uint64_t best = 0;
+    for (int c = 0; c < nchunk; ++c) best = src[c] > best ? src[c] : best;
+    const int32_t t = (int32_t)cand_id(best);
+    s_tgt[r] = t;
+    if (tgt_out != nullptr) tgt_out[o + r] = t;
+    s_tok[r] = token[o + r];
+    const int32_t p = parent[o + r];
+    s_par[r] = p;
+    s_mask[r] = mask[o + r];
+    s_leaf[r] = is_leaf[o + r];
+    if (r > 0 && (p < 0 || p >= r)) bad = true;
+  }
+  bad = __any_sync(kFull, bad);
+  __syncwarp();
+
+  int32_t* rows = accept_rows + (long)b * (S + 1);
+  int u = 0, L = 0;
+  if (!bad) {
+    for (;;) {
+      const int want = s_tgt[u];
+      int found = R;  // lowest matching child row
+      for (int base = 1; base < R; base += 32) {
+        const int c = base + lane;
+        const bool hit = c < R && s_par[c] == u && s_tok[c] == want;
+        const unsigned bal = __ballot_sync(kFull, hit);
+        if (bal && found == R) found = base + __ffs(bal) - 1;
+      }
+      if (found == R) break;
+      if (L == S) { bad = true; break; }
+      ++L;
+      if (lane == 0) rows[L] = found;
+      u = found;
+    }
+  }
+  if (bad) {
+    if (lane == 0) report_error(err, TSD_DEV_ERR_BAD_TREE, b);
+    u = 0;
+    L = 0;
+  }
+  __syncwarp();
+  for (int i = lane; i <= S; i += 32)
+    if (i == 0) rows[0] = 0;
+    else if (i > L) rows[i] = -1;
+
+  int chain = -1;
+  if (L > 0) {
+    for (int base = 1; base < R && chain < 0; base += 32) {
+      const int c = base + lane;
+      const bool hit = c < R && s_leaf[c] && ((s_mask[c] >> (u - 1)) & 1ull);
+      const unsigned bal = __ballot_sync(kFull, hit);
+      if (bal) chain = base + __ffs(bal) - 1;
+    }
+  }
+  if (lane == 0) {
+    accept_len[b] = L;
+    bonus[b] = s_tgt[u];
+    chain_id[b] = chain;
+  }
+}
+
+}  // namespace
+}  // namespace tsd
+
+using namespace tsd;
+
+extern "C" size_t tsd_accept_walk_workspace_size(int B, int D, int V) {
+  if (B < 1 || D < 0 || V < 1) return 0;
+  const long rows = (long)B * (D + 1);
+  const ScanGeom g = scan_geometry(rows, V);
+  return (size_t)rows * g.nchunk * sizeof(uint64_t);
+}
+
+extern "C" tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, int V,
+                                      const int32_t* token, const int32_t* parent,
+                                      const uint64_t* mask, const uint8_t* is_leaf,
+                                      int32_t* tgt, int32_t* accept_len, int32_t* accept_rows,
+                                      int32_t* bonus, int32_t* chain_id, void* ws,
+                                      size_t ws_bytes, int32_t* err, tsd_stream_t stream) {
+  if (B < 1 || D < 1 || D > kMaxR - 1 || S < 1 || S > 16 || V < 1 || V > (1 << 30))
+    return TSD_ERR_INVALID_ARG;
+  if ((long)B * (D + 1) > (1l << 24)) return TSD_ERR_INVALID_ARG;
+  if (!ok_ptr(logits) || !ok_ptr(token) || !ok_ptr(parent) || !ok_ptr(mask) ||
+      !ok_ptr(is_leaf) || !ok_opt_ptr(tgt) || !ok_ptr(accept_len) || !ok_ptr(accept_rows) ||
+      !ok_ptr(bonus) || !ok_ptr(chain_id) || !ok_opt_ptr(err))
+    return TSD_ERR_INVALID_ARG;
+  const size_t need = tsd_accept_walk_workspace_size(B, D, V);
+  if (ws_bytes < need || !ok_ptr(ws)) return TSD_ERR_INVALID_ARG;
+
+  const cudaStream_t st = (cudaStream_t)stream;
+  const int R = D + 1;
+  const long rows = (long)B * R;
+  const ScanGeom g = scan_geometry(rows, V);
+  uint64_t* part = (uint64_t*)ws;
+  vocab_scan_kernel<true><<<(unsigned)(rows * g.nchunk), kScanThreads, 0, st>>>(
+      logits, V, 1, g.nchunk, g.chunk_len, part);
+  accept_walk_kernel<<<B, 32, 0, st>>>(part, R, S, g.nchunk, token, parent, mask, is_leaf, tgt,
+                                       accept_len, accept_rows, bonus, chain_id, err);
+  return cuda_status();
+}

@@ -1,0 +1,79 @@
+// Device helpers shared by the verify-step kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tsd.h"
+
+namespace tsd {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Order-preserving map of an fp32 value to uint32 (larger float -> larger
+// key).  -0.0 is folded onto +0.0 so that the two compare equal, as they do
+// for float comparison.
+__device__ __forceinline__ uint32_t f32_order_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float order_key_f32(uint32_t k) {
+  const uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(u);
+}
+
+// A vocabulary candidate as one 64-bit integer: value in the high word,
+// bit-inverted token id in the low word.  A larger candidate is a larger
+// value, or an equal value with a smaller id -- the (value desc, id asc)
+// order of top-k and of argmax with ties to the lowest id.  Distinct ids give
+// distinct candidates.  0 is below every real candidate.
+__device__ __forceinline__ uint64_t make_cand(float x, uint32_t id) {
+  return ((uint64_t)f32_order_key(x) << 32) | (uint64_t)(~id);
+}
+__device__ __forceinline__ uint32_t cand_id(uint64_t c) { return ~(uint32_t)c; }
+__device__ __forceinline__ float cand_val(uint64_t c) { return order_key_f32((uint32_t)(c >> 32)); }
+
+// First device error wins; request index in the low 24 bits.
+__device__ __forceinline__ void report_error(int32_t* err, int code, int b) {
+  if (err != nullptr) atomicCAS(err, 0, code | (b & 0xffffff));
+}
+
+// Insert candidate c into a warp-distributed list sorted in descending order
+// (lane j holds the j-th largest; only lanes < k are meaningful).  The caller
+// guarantees c is larger than the current k-th entry, so c lands in [0, k).
+__device__ __forceinline__ void warp_list_insert(uint64_t& entry, uint64_t c, unsigned kmask, int lane) {
+  const unsigned greater = __ballot_sync(kFull, entry > c) & kmask;
+  const int pos = __popc(greater);
+  const uint64_t up = __shfl_up_sync(kFull, entry, 1);
+  if (lane > pos) entry = up;
+  else if (lane == pos) entry = c;
+}
+
+// Offer one candidate per lane to the warp list; `thr` (warp-uniform) is the
+// smallest key a new entry must beat and is raised as the list fills.
+__device__ __forceinline__ void warp_list_offer(uint64_t& entry, uint64_t& thr, uint64_t c, int k,
+                                                unsigned kmask, int lane) {
+  unsigned pending = __ballot_sync(kFull, c > thr);
+  while (pending) {
+    const int src = __ffs(pending) - 1;
+    pending &= pending - 1;
+    const uint64_t cc = __shfl_sync(kFull, c, src);
+    if (cc > thr) {
+      warp_list_insert(entry, cc, kmask, lane);
+      thr = __shfl_sync(kFull, entry, k - 1);
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t w = __shfl_xor_sync(kFull, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+}  // namespace tsd

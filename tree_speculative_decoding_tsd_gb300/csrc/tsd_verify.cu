@@ -1,0 +1,309 @@
+// tsd_tree_verify_attn: branch-aware tree attention over the shared prefix
+// KV cache plus each node's own ancestors in the scratch pad.
+//
+// Source: "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4"
+// (review), research gap item 1 (a candidate must see only its own
+// ancestors, never another branch; batch order and logical dependency
+// differ), "How it works" step 3 (A-B-B sees A and A-B, A-C sees only A) and
+// step 5 (all chains are verified in one target pass).
+//
+// Work decomposition (flash-decoding): the query rows of one KV head -- all
+// R tree rows x g query heads of the group ("packed rows") -- share every
+// prefix key, so a CTA takes a group of packed rows, one KV head and one
+// split of the prefix, and reads each prefix key once for all its rows.  The
+// CTA that owns the last split of a request also takes the R scratch-pad rows,
+// masked per packed row by the ancestor bitmask.  Partial results (normalised
+// output and log2-sum-exp per split) are merged by verify_combine_kernel; with
+// one split the attention kernel writes the final output directly.
+//
+// Paths:
+//   generic (this file): CUDA-core fp32 arithmetic, one warp per key, lanes
+//     split the head dim, warp-shuffle reductions for q.k; any dtype/dims.
+//     Used for fp32 inputs (never TF32) and for fewer than 64 packed rows.
+#include <math.h>
+
+#include <cuda_bf16.h>
+
+#include "tsd_common.cuh"
+#include "tsd_host.h"
+#include "tsd_verify.cuh"
+
+namespace tsd {
+namespace {
+
+constexpr int kGenThreads = 128;
+constexpr int kGenWarps = kGenThreads / 32;
+
+template <typename T> __device__ __forceinline__ float ldf(const T* p);
+template <> __device__ __forceinline__ float ldf<float>(const float* p) { return __ldg(p); }
+template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+template <typename T> __device__ __forceinline__ T cvt_out(float x);
+template <> __device__ __forceinline__ float cvt_out<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// One CTA: packed rows [rg*RB, rg*RB+RB) of KV head hk of request b, prefix
+// keys of split sp (and the tree rows if sp is the request's last split).
+template <typename T, int DK, int DV, int RB, bool ALIAS>
+__global__ void __launch_bounds__(kGenThreads)
+verify_generic_kernel(VerifyArgs a) {
+  constexpr int NK = DK / 32, NV = DV / 32;
+  __shared__ float sm_m[kGenWarps][RB], sm_l[kGenWarps][RB];
+  __shared__ float sm_o[kGenWarps][RB][DV];
+
+  const int sp = blockIdx.x;
+  const int hk = blockIdx.y / a.nrg, rg = blockIdx.y % a.nrg;
+  const int b = blockIdx.z;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int P = min(max(a.plen[b], 0), a.cap);  // out-of-range lengths never read past the cache
+  const int nsb = P > 0 ? (P + a.split_len - 1) / a.split_len : 1;
+  if (sp >= nsb) return;
+  const int k0 = sp * a.split_len, k1 = min(P, k0 + a.split_len);
+  const bool with_tree = (sp == nsb - 1);
+
+  float qv[RB][NK], o[RB][NV], m[RB], l[RB];
+  uint64_t rmask[RB];
+#pragma unroll
+  for (int i = 0; i < RB; ++i) {
+    const int p = rg * RB + i;
+    const bool valid = p < a.M;
+    const int r = valid ? p / a.g : 0, h = hk * a.g + (valid ? p % a.g : 0);
+    const T* qp = (const T*)a.q + (((long)b * a.R + r) * a.Hq + h) * DK;
+#pragma unroll
+    for (int t = 0; t < NK; ++t) qv[i][t] = valid ? ldf(qp + lane + 32 * t) * a.qscale : 0.f;
+    rmask[i] = (valid && r > 0) ? a.mask[(long)b * a.R + r] : 0ull;
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+#pragma unroll
+    for (int t = 0; t < NV; ++t) o[i][t] = 0.f;
+  }
+  const int nrows = min(RB, a.M - rg * RB);
+
+  auto visit = [&](const T* kp, const T* vp, bool is_tree, int j) {
+    float kv[NK], vv[NV];
+#pragma unroll
+    for (int t = 0; t < NK; ++t) kv[t] = ldf(kp + lane + 32 * t);
+#pragma unroll
+    for (int t = 0; t < NV; ++t) vv[t] = ldf(vp + lane + 32 * t);
+#pragma unroll
+    for (int i = 0; i < RB; ++i) {
+      if (i >= nrows) break;
+      float d = 0.f;
+#pragma unroll
+      for (int t = 0; t < NK; ++t) d = fmaf(qv[i][t], kv[t], d);
+      d = warp_sum(d);
+      if (is_tree && j > 0 && !((rmask[i] >> (j - 1)) & 1ull)) continue;
+      if (d > m[i]) {
+        const float al = exp2f(m[i] - d);
+        l[i] = fmaf(l[i], al, 1.f);
+#pragma unroll
+        for (int t = 0; t < NV; ++t) o[i][t] = fmaf(o[i][t], al, vv[t]);
+        m[i] = d;
+      } else {
+        const float pr = exp2f(d - m[i]);
+        l[i] += pr;
+#pragma unroll
+        for (int t = 0; t < NV; ++t) o[i][t] = fmaf(pr, vv[t], o[i][t]);
+      }
+    }
+  };
+
+  const long head = (long)b * a.Hkv + hk;
+  const T* kbase = (const T*)a.kc + head * a.cap * DK;
+  const T* vbase = ALIAS ? kbase : (const T*)a.vc + head * a.cap * DV;
+  constexpr int vstride = ALIAS ? DK : DV;
+  for (int j = k0 + warp; j < k1; j += kGenWarps)
+    visit(kbase + (long)j * DK, vbase + (long)j * vstride, false, j);
+  if (with_tree) {
+    const T* kt = (const T*)a.kt + ((long)b * a.R * a.Hkv + hk) * DK;
+    const T* vt = ALIAS ? kt : (const T*)a.vt + ((long)b * a.R * a.Hkv + hk) * DV;
+    for (int j = warp; j < a.R; j += kGenWarps)
+      visit(kt + (long)j * a.Hkv * DK, vt + (long)j * a.Hkv * vstride, true, j);
+  }
+
+  // merge the four warps' running states
+#pragma unroll
+  for (int i = 0; i < RB; ++i) {
+    if (lane == 0) { sm_m[warp][i] = m[i]; sm_l[warp][i] = l[i]; }
+#pragma unroll
+    for (int t = 0; t < NV; ++t) sm_o[warp][i][lane + 32 * t] = o[i][t];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < nrows * DV; idx += kGenThreads) {
+    const int i = idx / DV, c = idx - i * DV;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kGenWarps; ++w) mx = fmaxf(mx, sm_m[w][i]);
+    float lt = 0.f, ot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kGenWarps; ++w) {
+      const float wt = sm_m[w][i] == -INFINITY ? 0.f : exp2f(sm_m[w][i] - mx);
+      lt = fmaf(sm_l[w][i], wt, lt);
+      ot = fmaf(sm_o[w][i][c], wt, ot);
+    }
+    const float res = ot / lt;
+    const float lse2 = mx + log2f(lt);
+    const int p = rg * RB + i;
+    const int r = p / a.g, h = hk * a.g + p % a.g;
+    const long orow = ((long)b * a.R + r) * a.Hq + h;
+    if (a.nsplit == 1) {
+      ((T*)a.out)[orow * DV + c] = cvt_out<T>(res);
+      if (c == 0) a.lse[orow] = lse2 * 0.69314718055994531f;
+    } else {
+      const long prow = (((long)b * a.Hq + h) * a.R + r) * a.nsplit + sp;
+      a.ws_o[prow * DV + c] = res;
+      if (c == 0) a.ws_lse[prow] = lse2;
+    }
+  }
+}
+
+}  // namespace
+
+// Merge the per-split partials of every output row: one warp per
+// (b, r, h).  Weights are 2^(lse2_s - lse2_total).
+template <typename T, int DV>
+__global__ void __launch_bounds__(128) verify_combine_kernel(VerifyArgs a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long row = (long)blockIdx.x * 4 + warp;  // ((b*R + r)*Hq + h)
+  if (row >= (long)a.B * a.R * a.Hq) return;
+  const int b = (int)(row / ((long)a.R * a.Hq));
+  const int r = (int)((row / a.Hq) % a.R);
+  const int h = (int)(row % a.Hq);
+  const int P = min(max(a.plen[b], 0), a.cap);
+  const int nsb = P > 0 ? (P + a.split_len - 1) / a.split_len : 1;
+  const long base = (((long)b * a.Hq + h) * a.R + r) * a.nsplit;
+  float mx = -INFINITY;
+  for (int s = lane; s < nsb; s += 32) mx = fmaxf(mx, a.ws_lse[base + s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  float sum = 0.f;
+  for (int s = lane; s < nsb; s += 32) sum += exp2f(a.ws_lse[base + s] - mx);
+  sum = warp_sum(sum);
+  const float tot = mx + log2f(sum);
+  constexpr int NV = DV / 32;
+  float acc[NV];
+#pragma unroll
+  for (int t = 0; t < NV; ++t) acc[t] = 0.f;
+  for (int s = 0; s < nsb; ++s) {
+    const float w = exp2f(a.ws_lse[base + s] - tot);
+    const float* src = a.ws_o + (base + s) * DV;
+#pragma unroll
+    for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, src[lane + 32 * t], acc[t]);
+  }
+#pragma unroll
+  for (int t = 0; t < NV; ++t) ((T*)a.out)[row * DV + lane + 32 * t] = cvt_out<T>(acc[t]);
+  if (lane == 0) a.lse[row] = tot * 0.69314718055994531f;
+}
+
+// ---------------------------------------------------------------- planning --
+
+VerifyPlan plan_verify(const tsd_attn_desc& d) {
+  // The split of the prefix depends only on per-request quantities (never on
+  // B), so a request's result is bit-identical alone or inside any batch.
+  VerifyPlan p{};
+  p.path = kPathGeneric;
+  const int M = d.R * (d.Hq / d.Hkv);
+  p.rb = d.dk > 128 ? 2 : 8;
+  p.nrg = (int)ceil_div(M, p.rb);
+  const long per_request = (long)d.Hkv * p.nrg;
+  long ns = ceil_div(152L * 4, per_request);  // one request alone fills a wave
+  const long max_ns = ceil_div(d.cap, 256);
+  if (ns > max_ns) ns = max_ns;
+  if (ns < 1) ns = 1;
+  p.split_len = (int)ceil_div(d.cap, ns);
+  p.nsplit = (int)ceil_div(d.cap, p.split_len);
+  p.ws_bytes = p.nsplit > 1 ? (size_t)d.B * d.Hq * d.R * p.nsplit * (d.dv + 1) * sizeof(float) : 0;
+  return p;
+}
+
+template <typename T, int DK, int DV, int RB, bool ALIAS>
+static void launch_generic(const VerifyArgs& a, const VerifyPlan& p, cudaStream_t st) {
+  const dim3 grid(p.nsplit, a.Hkv * p.nrg, a.B);
+  verify_generic_kernel<T, DK, DV, RB, ALIAS><<<grid, kGenThreads, 0, st>>>(a);
+  if (p.nsplit > 1) {
+    const long rows = (long)a.B * a.R * a.Hq;
+    verify_combine_kernel<T, DV><<<(unsigned)ceil_div(rows, 4), 128, 0, st>>>(a);
+  }
+}
+
+bool launch_generic_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPlan& p,
+                         cudaStream_t st) {
+  const bool bf = d.dtype == TSD_BF16;
+  if (d.v_aliases_k) {
+    if (d.dk != 576 || d.dv != 512) return false;
+    if (bf) launch_generic<__nv_bfloat16, 576, 512, 2, true>(a, p, st);
+    else launch_generic<float, 576, 512, 2, true>(a, p, st);
+    return true;
+  }
+  if (d.dk != d.dv) return false;
+  if (d.dk == 128) {
+    if (bf) launch_generic<__nv_bfloat16, 128, 128, 8, false>(a, p, st);
+    else launch_generic<float, 128, 128, 8, false>(a, p, st);
+    return true;
+  }
+  if (d.dk == 64) {
+    if (bf) launch_generic<__nv_bfloat16, 64, 64, 8, false>(a, p, st);
+    else launch_generic<float, 64, 64, 8, false>(a, p, st);
+    return true;
+  }
+  return false;
+}
+
+}  // namespace tsd
+
+using namespace tsd;
+
+static bool desc_ok(const tsd_attn_desc* d) {
+  if (d == nullptr) return false;
+  if (d->B < 1 || d->B > 65535 || d->R < 1 || d->R > 65 || d->Hq < 1 || d->Hkv < 1 ||
+      d->Hq % d->Hkv != 0 || d->cap < 1)
+    return false;
+  if (d->dtype != TSD_F32 && d->dtype != TSD_BF16) return false;
+  if (!(d->scale > 0.f) || !(d->scale < 1e30f)) return false;
+  const bool mla = d->v_aliases_k && d->dk == 576 && d->dv == 512;
+  const bool gqa = !d->v_aliases_k && d->dk == d->dv && (d->dk == 64 || d->dk == 128);
+  return mla || gqa;
+}
+
+extern "C" size_t tsd_verify_workspace_size(const tsd_attn_desc* d) {
+  if (!desc_ok(d)) return 0;
+  return plan_verify(*d).ws_bytes;
+}
+
+extern "C" tsd_status tsd_tree_verify_attn(const tsd_attn_desc* d, const void* q,
+                                           const void* kcache, const void* vcache,
+                                           const int32_t* prefix_len, const void* ktree,
+                                           const void* vtree, const uint64_t* mask, void* out,
+                                           float* lse, void* ws, size_t ws_bytes, int32_t* err,
+                                           tsd_stream_t stream) {
+  (void)err;
+  if (!desc_ok(d)) return TSD_ERR_INVALID_ARG;
+  if (!ok_ptr(q) || !ok_ptr(kcache) || !ok_ptr(prefix_len) || !ok_ptr(ktree) || !ok_ptr(mask) ||
+      !ok_ptr(out) || !ok_ptr(lse))
+    return TSD_ERR_INVALID_ARG;
+  if (!d->v_aliases_k && (!ok_ptr(vcache) || !ok_ptr(vtree))) return TSD_ERR_INVALID_ARG;
+  const VerifyPlan p = plan_verify(*d);
+  if (ws_bytes < p.ws_bytes || (p.ws_bytes > 0 && !ok_ptr(ws))) return TSD_ERR_INVALID_ARG;
+
+  VerifyArgs a{};
+  a.q = q; a.kc = kcache; a.vc = vcache; a.plen = prefix_len;
+  a.kt = ktree; a.vt = vtree; a.mask = mask;
+  a.out = out; a.lse = lse;
+  a.ws_o = (float*)ws;
+  a.ws_lse = p.nsplit > 1 ? (float*)ws + (size_t)d->B * d->Hq * d->R * p.nsplit * d->dv : nullptr;
+  a.B = d->B; a.R = d->R; a.Hq = d->Hq; a.Hkv = d->Hkv; a.g = d->Hq / d->Hkv;
+  a.M = d->R * a.g; a.cap = d->cap;
+  a.nsplit = p.nsplit; a.split_len = p.split_len; a.nrg = p.nrg;
+  a.qscale = d->scale * 1.4426950408889634f;
+  if (!launch_generic_path(*d, a, p, (cudaStream_t)stream)) return TSD_ERR_UNSUPPORTED;
+  return cuda_status();
+}

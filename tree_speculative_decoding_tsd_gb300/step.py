@@ -1,0 +1,99 @@
+"""One tree-verify step: device buffers plus the four C-ABI calls on one stream.
+
+``TreeVerifyStep`` owns every output and workspace buffer of the step for a
+fixed configuration, so repeated steps allocate nothing.  The inputs of a
+step (draft marginals, root tokens, queries, scratch-pad K/V, target logits)
+and the persistent state (KV cache, prefix lengths) are caller tensors.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from . import (make_desc, tsd_accept_walk, tsd_accept_walk_workspace_size, tsd_commit_path,
+               tsd_tree_build, tsd_tree_build_workspace_size, tsd_tree_verify_attn,
+               tsd_verify_workspace_size, workspace)
+
+
+@dataclasses.dataclass
+class TreeBuffers:
+    token: torch.Tensor
+    parent: torch.Tensor
+    depth: torch.Tensor
+    score: torch.Tensor
+    mask: torch.Tensor
+    is_leaf: torch.Tensor
+
+
+@dataclasses.dataclass
+class WalkBuffers:
+    tgt: torch.Tensor
+    accept_len: torch.Tensor
+    accept_rows: torch.Tensor
+    bonus: torch.Tensor
+    chain_id: torch.Tensor
+
+
+class TreeVerifyStep:
+    def __init__(self, B, S, V, k, D, Hq, Hkv, dk, dv, cap, dtype, v_aliases_k, scale,
+                 device="cuda"):
+        self.B, self.S, self.V, self.k, self.D = B, S, V, k, D
+        self.R = R = D + 1
+        self.Hq, self.Hkv, self.dk, self.dv, self.cap = Hq, Hkv, dk, dv, cap
+        self.dtype = dtype
+        self.v_aliases_k = v_aliases_k
+        self.desc = make_desc(B, R, Hq, Hkv, dk, dv, cap, dtype, v_aliases_k, scale)
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.tree = TreeBuffers(
+            token=torch.empty((B, R), **i32), parent=torch.empty((B, R), **i32),
+            depth=torch.empty((B, R), **i32),
+            score=torch.empty((B, R), dtype=torch.float32, device=dev),
+            mask=torch.empty((B, R), dtype=torch.int64, device=dev),   # uint64 bit patterns
+            is_leaf=torch.empty((B, R), dtype=torch.uint8, device=dev))
+        self.out = torch.empty((B, R, Hq, dv), dtype=dtype, device=dev)
+        self.lse = torch.empty((B, R, Hq), dtype=torch.float32, device=dev)
+        self.walk = WalkBuffers(
+            tgt=torch.empty((B, R), **i32), accept_len=torch.empty((B,), **i32),
+            accept_rows=torch.empty((B, S + 1), **i32), bonus=torch.empty((B,), **i32),
+            chain_id=torch.empty((B,), **i32))
+        self.err = torch.zeros((4,), **i32)
+        self.ws_build = workspace(tsd_tree_build_workspace_size(B, S, V, k), dev)
+        self.ws_verify = workspace(tsd_verify_workspace_size(self.desc), dev)
+        self.ws_walk = workspace(tsd_accept_walk_workspace_size(B, D, V), dev)
+
+    # the four calls -------------------------------------------------------
+    def build(self, probs, root_tok, stream=None):
+        t = self.tree
+        tsd_tree_build(probs, self.k, self.D, root_tok, t.token, t.parent, t.depth, t.score,
+                       t.mask, t.is_leaf, self.ws_build, self.err, stream)
+
+    def verify(self, q, kcache, vcache, prefix_len, ktree, vtree, stream=None):
+        tsd_tree_verify_attn(self.desc, q, kcache, vcache, prefix_len, ktree, vtree,
+                             self.tree.mask, self.out, self.lse, self.ws_verify, self.err, stream)
+
+    def accept(self, logits, stream=None):
+        t, w = self.tree, self.walk
+        tsd_accept_walk(logits, self.S, t.token, t.parent, t.mask, t.is_leaf, w.tgt,
+                        w.accept_len, w.accept_rows, w.bonus, w.chain_id, self.ws_walk, self.err,
+                        stream)
+
+    def commit(self, ktree, vtree, kcache, vcache, prefix_len, stream=None):
+        w = self.walk
+        tsd_commit_path(self.desc, self.S, ktree, vtree, w.accept_rows, w.accept_len, kcache,
+                        vcache, prefix_len, self.err, stream)
+
+    def run(self, probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits,
+            stream=None):
+        """The whole step: build -> verify -> accept -> commit (asynchronous)."""
+        self.build(probs, root_tok, stream)
+        self.verify(q, kcache, vcache, prefix_len, ktree, vtree, stream)
+        self.accept(logits, stream)
+        self.commit(ktree, vtree, kcache, vcache, prefix_len, stream)
+
+    @classmethod
+    def for_workload(cls, w, device="cuda"):
+        return cls(w.B, w.S, w.V, w.k, w.D, w.Hq, w.Hkv, w.dk, w.dv, w.cap, w.torch_dtype,
+                   w.v_aliases_k, w.scale, device)
