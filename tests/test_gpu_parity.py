@@ -161,6 +161,7 @@ def check_attention(w, q, kc, vc, plen, kt, vt, mask, sel=None):
 
 def sample_rows(w, n, seed=0):
     rng = np.random.default_rng(seed)
+    n = min(n, w.B * w.R * w.Hq)
     rows = {(0, 0, 0), (w.B - 1, w.R - 1, w.Hq - 1), (0, w.R - 1, w.Hq // 2), (w.B - 1, 1, 0)}
     while len(rows) < n:
         rows.add((int(rng.integers(w.B)), int(rng.integers(w.R)), int(rng.integers(w.Hq))))

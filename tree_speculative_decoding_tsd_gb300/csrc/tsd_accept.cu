@@ -38,14 +38,29 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
   const int lane = threadIdx.x;
   const long o = (long)b * R;
 
+  // tgt[r]: the largest of the row's chunk maxima (lanes split the chunks)
+  for (int r0 = 0; r0 < R; r0 += 4) {
+    uint64_t best[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      best[u] = 0ull;
+      if (r0 + u < R) {
+        const uint64_t* src = part + (o + r0 + u) * nchunk;
+        for (int c = lane; c < nchunk; c += 32) best[u] = src[c] > best[u] ? src[c] : best[u];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint64_t m = warp_max_u64(best[u]);
+      if (lane == 0 && r0 + u < R) {
+        const int32_t t = (int32_t)cand_id(m);
+        s_tgt[r0 + u] = t;
+        if (tgt_out != nullptr) tgt_out[o + r0 + u] = t;
+      }
+    }
+  }
   bool bad = false;
   for (int r = lane; r < R; r += 32) {
-    const uint64_t* src = part + (o + r) * nchunk;
-    uint64_t best = 0;
-    for (int c = 0; c < nchunk; ++c) best = src[c] > best ? src[c] : best;
-    const int32_t t = (int32_t)cand_id(best);
-    s_tgt[r] = t;
-    if (tgt_out != nullptr) tgt_out[o + r] = t;
     s_tok[r] = token[o + r];
     const int32_t p = parent[o + r];
     s_par[r] = p;
@@ -109,7 +124,7 @@ using namespace tsd;
 extern "C" size_t tsd_accept_walk_workspace_size(int B, int D, int V) {
   if (B < 1 || D < 0 || V < 1) return 0;
   const long rows = (long)B * (D + 1);
-  const ScanGeom g = scan_geometry(rows, V);
+  const ScanGeom g = scan_geometry(rows, V, 1);
   return (size_t)rows * g.nchunk * sizeof(uint64_t);
 }
 
@@ -132,7 +147,7 @@ extern "C" tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, 
   const cudaStream_t st = (cudaStream_t)stream;
   const int R = D + 1;
   const long rows = (long)B * R;
-  const ScanGeom g = scan_geometry(rows, V);
+  const ScanGeom g = scan_geometry(rows, V, 1);
   uint64_t* part = (uint64_t*)ws;
   vocab_scan_kernel<true><<<(unsigned)(rows * g.nchunk), kScanThreads, 0, st>>>(
       logits, V, 1, g.nchunk, g.chunk_len, part);

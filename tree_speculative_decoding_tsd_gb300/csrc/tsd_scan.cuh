@@ -25,16 +25,20 @@ constexpr int kScanWarps = kScanThreads / 32;
 // Partitioning assumes the GB300's 152 SMs with 8 resident scan CTAs each.
 constexpr int kScanTargetCtas = 152 * 8;
 constexpr int kScanMinChunk = 2048;
+// A row's chunk lists hold at most this many candidates, so the merge in the
+// consumer kernel reads a short, fixed-size list per row.
+constexpr int kScanMaxCand = 256;
 
 struct ScanGeom {
   int nchunk;
   int chunk_len;  // multiple of 256 elements
 };
 
-inline ScanGeom scan_geometry(long rows, int V) {
+inline ScanGeom scan_geometry(long rows, int V, int k) {
   long per_row = (kScanTargetCtas + rows - 1) / rows;
   long max_chunks = (V + kScanMinChunk - 1) / kScanMinChunk;
   if (per_row > max_chunks) per_row = max_chunks;
+  if (per_row > kScanMaxCand / k) per_row = kScanMaxCand / k;
   if (per_row < 1) per_row = 1;
   long len = (V + per_row - 1) / per_row;
   len = (len + 255) / 256 * 256;
@@ -71,9 +75,14 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
   const float4* xv = reinterpret_cast<const float4*>(xr + a0);
 
   if (kArgmax) {
-    uint64_t best = 0;
-    for (int i = c0 + tid; i < a0; i += kScanThreads) { const uint64_t c = make_cand(xr[i], i); best = c > best ? c : best; }
-    for (int i = a1 + tid; i < c1; i += kScanThreads) { const uint64_t c = make_cand(xr[i], i); best = c > best ? c : best; }
+    // Each thread visits its elements in increasing index order and keeps the
+    // first maximum (strict >); threads are then merged by (value, id) keys.
+    float bx = -INFINITY;
+    int bi = -1;
+    auto take = [&](float x, int i) {
+      if (x > bx || bi < 0) { bx = x; bi = i; }
+    };
+    for (int i = c0 + tid; i < a0; i += kScanThreads) take(xr[i], i);
     int v = tid;
     for (; v + 3 * kScanThreads < nvec; v += 4 * kScanThreads) {
       float4 f[4];
@@ -81,23 +90,27 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
       for (int u = 0; u < 4; ++u) f[u] = ld_stream(xv + v + u * kScanThreads);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const uint32_t i0 = (uint32_t)(a0 + 4 * (v + u * kScanThreads));
-        uint64_t c;
-        c = make_cand(f[u].x, i0);     best = c > best ? c : best;
-        c = make_cand(f[u].y, i0 + 1); best = c > best ? c : best;
-        c = make_cand(f[u].z, i0 + 2); best = c > best ? c : best;
-        c = make_cand(f[u].w, i0 + 3); best = c > best ? c : best;
+        const int i0 = a0 + 4 * (v + u * kScanThreads);
+        take(f[u].x, i0); take(f[u].y, i0 + 1); take(f[u].z, i0 + 2); take(f[u].w, i0 + 3);
       }
     }
-    for (; v < nvec; v += kScanThreads) {
-      const float4 f = ld_stream(xv + v);
-      const uint32_t i0 = (uint32_t)(a0 + 4 * v);
-      uint64_t c;
-      c = make_cand(f.x, i0);     best = c > best ? c : best;
-      c = make_cand(f.y, i0 + 1); best = c > best ? c : best;
-      c = make_cand(f.z, i0 + 2); best = c > best ? c : best;
-      c = make_cand(f.w, i0 + 3); best = c > best ? c : best;
+    {
+      float4 f[3];
+      bool have[3];
+#pragma unroll
+      for (int u = 0; u < 3; ++u) {
+        have[u] = v + u * kScanThreads < nvec;
+        if (have[u]) f[u] = ld_stream(xv + v + u * kScanThreads);
+      }
+#pragma unroll
+      for (int u = 0; u < 3; ++u) {
+        if (!have[u]) continue;
+        const int i0 = a0 + 4 * (v + u * kScanThreads);
+        take(f[u].x, i0); take(f[u].y, i0 + 1); take(f[u].z, i0 + 2); take(f[u].w, i0 + 3);
+      }
     }
+    for (int i = a1 + tid; i < c1; i += kScanThreads) take(xr[i], i);
+    uint64_t best = bi < 0 ? 0ull : make_cand(bx, (uint32_t)bi);
     best = warp_max_u64(best);
     if (lane == 0) s_list[warp][0] = best;
     __syncthreads();
@@ -139,18 +152,15 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
       have[u] = v < nvec;
       f[u] = have[u] ? ld_stream(xv + v) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    // quick reject on the 32-bit value key
-    const uint32_t thr_hi = (uint32_t)(thr >> 32);
-    uint32_t hi = 0;
+    // quick reject: nothing below the threshold's value can enter the list
+    const float thr_v = thr == 0ull ? -INFINITY : cand_val(thr);
+    float hi = -INFINITY;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if (!have[u]) continue;
-      hi = max(hi, f32_order_key(f[u].x));
-      hi = max(hi, f32_order_key(f[u].y));
-      hi = max(hi, f32_order_key(f[u].z));
-      hi = max(hi, f32_order_key(f[u].w));
+      hi = fmaxf(hi, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
     }
-    if (__any_sync(kFull, hi >= thr_hi)) {
+    if (__any_sync(kFull, hi >= thr_v)) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint32_t i0 = (uint32_t)(a0 + 4 * (v0 + u * kScanThreads + lane));

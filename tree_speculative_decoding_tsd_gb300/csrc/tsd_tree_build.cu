@@ -12,8 +12,8 @@
 //
 // K1 vocab_scan_kernel<false>: per-chunk top-k of every (request, position)
 //    row, HBM-bound (see tsd_scan.cuh).
-// K2 best_first_tree_kernel: one warp per request.  Merges the chunk lists
-//    into the k best tokens of each position, then pops D nodes from a
+// K2 best_first_tree_kernel: one CTA per request; warp p merges the chunk lists
+//    of position p into its k best tokens, then warp 0 pops D nodes from a
 //    frontier.  Popping a node pushes its first child and its next sibling
 //    (children are the top-k of the next position in rank order, so a node's
 //    first child and younger siblings never precede it); this visits nodes in
@@ -59,7 +59,7 @@ __device__ __forceinline__ bool precedes(const TreeSmem& s, int a, int b) {
   return s.f_w1[a] < s.f_w1[b];
 }
 
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(32 * kMaxS)
 best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, int nchunk,
                        const int32_t* __restrict__ root_tok, int32_t* __restrict__ token,
                        int32_t* __restrict__ parent, int32_t* __restrict__ depth,
@@ -67,25 +67,37 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
                        uint8_t* __restrict__ is_leaf) {
   __shared__ TreeSmem s;
   const int b = blockIdx.x;
-  const int lane = threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = D + 1;
   const long o = (long)b * R;
   const unsigned kmask = (k >= 32) ? kFull : ((1u << k) - 1u);
 
-  // ---- merge the per-chunk lists into the top-k of each position ----
-  const int ncand = nchunk * k;
-  for (int p = 0; p < S; ++p) {
+  // ---- warp p merges the chunk lists of position p into its top-k ----
+  // (at most kScanMaxCand candidates: every lane loads its share up front)
+  {
+    const int p = warp;
+    const int ncand = nchunk * k;
     const uint64_t* src = part + ((long)b * S + p) * ncand;
+    constexpr int kPer = kScanMaxCand / 32;
+    uint64_t c[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = lane + 32 * j;
+      c[j] = i < ncand ? src[i] : 0ull;
+    }
     uint64_t entry = 0, thr = 0;
-    for (int base = 0; base < ncand; base += 32) {
-      const uint64_t c = base + lane < ncand ? src[base + lane] : 0ull;
-      warp_list_offer(entry, thr, c, k, kmask, lane);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (32 * j >= ncand) break;
+      warp_list_offer(entry, thr, c[j], k, kmask, lane);
     }
     if (lane < k) {
       s.tp[p][lane] = cand_val(entry);
       s.ti[p][lane] = (int32_t)cand_id(entry);
     }
   }
+  __syncthreads();
+  if (warp != 0) return;
 
   // ---- root row and the first frontier entry (rank 0 at depth 1) ----
   if (lane == 0) {
@@ -188,7 +200,7 @@ using namespace tsd;
 
 extern "C" size_t tsd_tree_build_workspace_size(int B, int S, int V, int k) {
   if (B < 1 || S < 1 || V < 1 || k < 1) return 0;
-  const ScanGeom g = scan_geometry((long)B * S, V);
+  const ScanGeom g = scan_geometry((long)B * S, V, k);
   return (size_t)B * S * g.nchunk * k * sizeof(uint64_t);
 }
 
@@ -209,12 +221,12 @@ extern "C" tsd_status tsd_tree_build(const float* probs, int B, int S, int V, in
   if (ws_bytes < need || !ok_ptr(ws)) return TSD_ERR_INVALID_ARG;
 
   const cudaStream_t st = (cudaStream_t)stream;
-  const ScanGeom g = scan_geometry((long)B * S, V);
+  const ScanGeom g = scan_geometry((long)B * S, V, k);
   const long ctas = (long)B * S * g.nchunk;
   uint64_t* part = (uint64_t*)ws;
   vocab_scan_kernel<false><<<(unsigned)ctas, kScanThreads, 0, st>>>(probs, V, k, g.nchunk,
                                                                     g.chunk_len, part);
-  best_first_tree_kernel<<<B, 32, 0, st>>>(part, S, k, D, g.nchunk, root_tok, token, parent,
+  best_first_tree_kernel<<<B, 32 * S, 0, st>>>(part, S, k, D, g.nchunk, root_tok, token, parent,
                                            depth, score, mask, is_leaf);
   return cuda_status();
 }

@@ -19,7 +19,10 @@
 // Paths:
 //   generic (this file): CUDA-core fp32 arithmetic, one warp per key, lanes
 //     split the head dim, warp-shuffle reductions for q.k; any dtype/dims.
-//     Used for fp32 inputs (never TF32) and for fewer than 64 packed rows.
+//     Used for fp32 inputs (never TF32), for fewer than 64 packed rows (not
+//     a dense contraction) and for the latent (dk 576 / dv 512) heads.
+//   mma (tsd_verify_mma.cu): bf16 GQA heads with >= 64 packed rows, both
+//     products on the tensor cores.
 #include <math.h>
 
 #include <cuda_bf16.h>
@@ -39,18 +42,6 @@ template <> __device__ __forceinline__ float ldf<float>(const float* p) { return
 template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) {
   return __bfloat162float(*p);
 }
-template <typename T> __device__ __forceinline__ T cvt_out(float x);
-template <> __device__ __forceinline__ float cvt_out<float>(float x) { return x; }
-template <> __device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(float x) {
-  return __float2bfloat16_rn(x);
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
-
 // One CTA: packed rows [rg*RB, rg*RB+RB) of KV head hk of request b, prefix
 // keys of split sp (and the tree rows if sp is the request's last split).
 template <typename T, int DK, int DV, int RB, bool ALIAS>
@@ -168,58 +159,36 @@ verify_generic_kernel(VerifyArgs a) {
 
 }  // namespace
 
-// Merge the per-split partials of every output row: one warp per
-// (b, r, h).  Weights are 2^(lse2_s - lse2_total).
-template <typename T, int DV>
-__global__ void __launch_bounds__(128) verify_combine_kernel(VerifyArgs a) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long row = (long)blockIdx.x * 4 + warp;  // ((b*R + r)*Hq + h)
-  if (row >= (long)a.B * a.R * a.Hq) return;
-  const int b = (int)(row / ((long)a.R * a.Hq));
-  const int r = (int)((row / a.Hq) % a.R);
-  const int h = (int)(row % a.Hq);
-  const int P = min(max(a.plen[b], 0), a.cap);
-  const int nsb = P > 0 ? (P + a.split_len - 1) / a.split_len : 1;
-  const long base = (((long)b * a.Hq + h) * a.R + r) * a.nsplit;
-  float mx = -INFINITY;
-  for (int s = lane; s < nsb; s += 32) mx = fmaxf(mx, a.ws_lse[base + s]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-  float sum = 0.f;
-  for (int s = lane; s < nsb; s += 32) sum += exp2f(a.ws_lse[base + s] - mx);
-  sum = warp_sum(sum);
-  const float tot = mx + log2f(sum);
-  constexpr int NV = DV / 32;
-  float acc[NV];
-#pragma unroll
-  for (int t = 0; t < NV; ++t) acc[t] = 0.f;
-  for (int s = 0; s < nsb; ++s) {
-    const float w = exp2f(a.ws_lse[base + s] - tot);
-    const float* src = a.ws_o + (base + s) * DV;
-#pragma unroll
-    for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, src[lane + 32 * t], acc[t]);
-  }
-#pragma unroll
-  for (int t = 0; t < NV; ++t) ((T*)a.out)[row * DV + lane + 32 * t] = cvt_out<T>(acc[t]);
-  if (lane == 0) a.lse[row] = tot * 0.69314718055994531f;
-}
-
 // ---------------------------------------------------------------- planning --
 
 VerifyPlan plan_verify(const tsd_attn_desc& d) {
   // The split of the prefix depends only on per-request quantities (never on
   // B), so a request's result is bit-identical alone or inside any batch.
   VerifyPlan p{};
-  p.path = kPathGeneric;
   const int M = d.R * (d.Hq / d.Hkv);
-  p.rb = d.dk > 128 ? 2 : 8;
-  p.nrg = (int)ceil_div(M, p.rb);
-  const long per_request = (long)d.Hkv * p.nrg;
-  long ns = ceil_div(152L * 4, per_request);  // one request alone fills a wave
-  const long max_ns = ceil_div(d.cap, 256);
-  if (ns > max_ns) ns = max_ns;
-  if (ns < 1) ns = 1;
-  p.split_len = (int)ceil_div(d.cap, ns);
+  const bool mma = d.dtype == TSD_BF16 && !d.v_aliases_k && d.dk == d.dv &&
+                   (d.dk == 64 || d.dk == 128) && M >= kMmaMinRows;
+  long ns;
+  if (mma) {
+    // one warp per 16 packed rows, at most 8 warps per CTA, balanced groups
+    p.path = kPathMma;
+    const int nblk = (int)ceil_div(M, 16);
+    p.nrg = (int)ceil_div(nblk, 8);
+    p.rb = (int)ceil_div(nblk, p.nrg) * 16;
+    ns = ceil_div(152L * 2, (long)d.Hkv * p.nrg);       // about two CTAs per SM for one request
+    long len = ceil_div(d.cap, ns);
+    len = ceil_div(len < 256 ? 256 : len, 64) * 64;       // whole 64-key tiles, >= 4 per split
+    p.split_len = (int)len;
+  } else {
+    p.path = kPathGeneric;
+    p.rb = d.dk > 128 ? 2 : 8;
+    p.nrg = (int)ceil_div(M, p.rb);
+    ns = ceil_div(152L * 4, (long)d.Hkv * p.nrg);
+    const long max_ns = ceil_div(d.cap, 256);
+    if (ns > max_ns) ns = max_ns;
+    if (ns < 1) ns = 1;
+    p.split_len = (int)ceil_div(d.cap, ns);
+  }
   p.nsplit = (int)ceil_div(d.cap, p.split_len);
   p.ws_bytes = p.nsplit > 1 ? (size_t)d.B * d.Hq * d.R * p.nsplit * (d.dv + 1) * sizeof(float) : 0;
   return p;
@@ -304,6 +273,9 @@ extern "C" tsd_status tsd_tree_verify_attn(const tsd_attn_desc* d, const void* q
   a.M = d->R * a.g; a.cap = d->cap;
   a.nsplit = p.nsplit; a.split_len = p.split_len; a.nrg = p.nrg;
   a.qscale = d->scale * 1.4426950408889634f;
-  if (!launch_generic_path(*d, a, p, (cudaStream_t)stream)) return TSD_ERR_UNSUPPORTED;
+  const cudaStream_t st = (cudaStream_t)stream;
+  const bool launched = p.path == kPathMma ? launch_mma_path(*d, a, p, st)
+                                           : launch_generic_path(*d, a, p, st);
+  if (!launched) return TSD_ERR_UNSUPPORTED;
   return cuda_status();
 }

@@ -1,10 +1,14 @@
 // Shared declarations of the tree-verify attention paths.
 #pragma once
 
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
 #include <stddef.h>
 #include <stdint.h>
 
 #include "tsd.h"
+#include "tsd_common.cuh"
 
 namespace tsd {
 
@@ -38,6 +42,64 @@ struct VerifyPlan {
   size_t ws_bytes;
 };
 
+// Fewer packed rows than this are not a dense contraction: CUDA cores.
+constexpr int kMmaMinRows = 64;
+
 VerifyPlan plan_verify(const tsd_attn_desc& d);
+bool launch_mma_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPlan& p,
+                     cudaStream_t st);
+
+namespace {
+
+template <typename T> __device__ __forceinline__ T cvt_out(float x);
+template <> __device__ __forceinline__ float cvt_out<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// Merge the per-split partials of every output row: one warp per (b, r, h).
+// Each split s left a normalised output O_s and its log2-sum-exp L_s; the
+// result is sum_s 2^(L_s - L) O_s with L = log2 sum_s 2^(L_s).
+template <typename T, int DV>
+__global__ void __launch_bounds__(128) verify_combine_kernel(VerifyArgs a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long row = (long)blockIdx.x * 4 + warp;  // ((b*R + r)*Hq + h)
+  if (row >= (long)a.B * a.R * a.Hq) return;
+  const int b = (int)(row / ((long)a.R * a.Hq));
+  const int r = (int)((row / a.Hq) % a.R);
+  const int h = (int)(row % a.Hq);
+  const int P = min(max(a.plen[b], 0), a.cap);
+  const int nsb = P > 0 ? (P + a.split_len - 1) / a.split_len : 1;
+  const long base = (((long)b * a.Hq + h) * a.R + r) * a.nsplit;
+  float mx = -INFINITY;
+  for (int s = lane; s < nsb; s += 32) mx = fmaxf(mx, a.ws_lse[base + s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  float sum = 0.f;
+  for (int s = lane; s < nsb; s += 32) sum += exp2f(a.ws_lse[base + s] - mx);
+  sum = warp_sum(sum);
+  const float tot = mx + log2f(sum);
+  constexpr int NV = DV / 32;
+  float acc[NV];
+#pragma unroll
+  for (int t = 0; t < NV; ++t) acc[t] = 0.f;
+  for (int s = 0; s < nsb; ++s) {
+    const float w = exp2f(a.ws_lse[base + s] - tot);
+    const float* src = a.ws_o + (base + s) * DV;
+#pragma unroll
+    for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, src[lane + 32 * t], acc[t]);
+  }
+#pragma unroll
+  for (int t = 0; t < NV; ++t) ((T*)a.out)[row * DV + lane + 32 * t] = cvt_out<T>(acc[t]);
+  if (lane == 0) a.lse[row] = tot * 0.69314718055994531f;
+}
+
+}  // namespace
 
 }  // namespace tsd
