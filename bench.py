@@ -210,7 +210,8 @@ def source_digest(files):
 
 CALL_SOURCES = {
     "build": ["tsd_tree_build.cu", "tsd_scan.cuh", "tsd_common.cuh"],
-    "verify": ["tsd_verify.cu", "tsd_verify.cuh", "tsd_common.cuh"],
+    "verify": ["tsd_verify.cu", "tsd_verify_tc.cu", "tsd_verify_mma.cu", "tsd_verify.cuh",
+               "tsd_common.cuh"],
     "accept": ["tsd_accept.cu", "tsd_scan.cuh", "tsd_common.cuh"],
     "commit": ["tsd_commit.cu", "tsd_common.cuh"],
 }

@@ -429,3 +429,60 @@ def test_full_step_chained(name, over):
         np.testing.assert_array_equal(W.bits(g[4].cpu()), vc_ref)
     np.testing.assert_array_equal(g[5].cpu().numpy(), pl_ref)
     assert int(step.err[0]) == 0
+
+
+# ------------------------------------------------- every attention path --
+
+@pytest.fixture
+def force_path(request):
+    import os
+    old = os.environ.get("TSD_VERIFY_PATH")
+    os.environ["TSD_VERIFY_PATH"] = request.param
+    yield request.param
+    if old is None:
+        os.environ.pop("TSD_VERIFY_PATH", None)
+    else:
+        os.environ["TSD_VERIFY_PATH"] = old
+
+
+@pytest.mark.parametrize("force_path", ["tc", "mma", "generic"], indirect=True)
+@pytest.mark.parametrize("key", ["qwen", "batched", "long"])
+def test_verify_each_path_reduced(force_path, key):
+    d = inputs(key, **REDUCED[key])
+    w = d["w"]
+    check_attention(w, *attn_inputs(w), d["tree"]["mask"])
+
+
+@pytest.mark.parametrize("force_path", ["tc", "mma"], indirect=True)
+@pytest.mark.parametrize("D", [15, 19, 23, 27, 31, 35, 48])
+def test_verify_tensor_core_column_tiles(force_path, D):
+    """Packed-row counts 64..196 (g = 4): every MMA N width and a two-group split."""
+    d = inputs("qwen", D=D, P=1300, P_min=1300, V=3000)
+    w = d["w"]
+    check_attention(w, *attn_inputs(w), d["tree"]["mask"])
+
+
+@pytest.mark.parametrize("force_path", ["tc", "mma", "generic"], indirect=True)
+def test_verify_rescale_on_late_large_scores(force_path):
+    """Keys near the end of the prefix align with the queries, so the running
+    max jumps on late tiles (exercises the rescale of the accumulators)."""
+    d = inputs("qwen", B=2, P=1500, P_min=1500, V=3000)
+    w, tree = d["w"], d["tree"]
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    g = w.Hq // w.Hkv
+    for b in range(w.B):
+        for hk in range(w.Hkv):
+            qd = q[b, :, hk * g:(hk + 1) * g].float().mean(dim=(0, 1))
+            qd = qd / qd.norm()
+            for j, pos in enumerate(range(1100, 1500, 37)):
+                kc[b, hk, pos] = (qd * (8.0 + j)).to(kc.dtype)
+    check_attention(w, q, kc, vc, plen, kt, vt, tree["mask"])
+
+
+@pytest.mark.parametrize("force_path", ["tc", "mma"], indirect=True)
+def test_verify_paths_empty_and_tiny_prefixes(force_path):
+    w = W.WORKLOADS["qwen"].scaled(B=6, P=300, P_min=0, V=500)
+    d = inputs("qwen", B=6, P=300, P_min=0, V=500)
+    q, kc, vc, _, kt, vt = attn_inputs(w)
+    plen = torch.tensor([0, 1, 127, 128, 129, 300], dtype=torch.int32)
+    check_attention(w, q, kc, vc, plen, kt, vt, d["tree"]["mask"])

@@ -21,9 +21,13 @@
 //     split the head dim, warp-shuffle reductions for q.k; any dtype/dims.
 //     Used for fp32 inputs (never TF32), for fewer than 64 packed rows (not
 //     a dense contraction) and for the latent (dk 576 / dv 512) heads.
-//   mma (tsd_verify_mma.cu): bf16 GQA heads with >= 64 packed rows, both
-//     products on the tensor cores.
+//   tc (tsd_verify_tc.cu): bf16 GQA heads, head dim 128, >= 64 packed rows:
+//     tcgen05 MMAs with TMEM accumulators, TMA-fed K/V ring (the default).
+//   mma (tsd_verify_mma.cu): bf16 GQA heads (head dim 64 or 128) with >= 64
+//     packed rows on the legacy warp-level mma.sync tensor-core path.
 #include <math.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <cuda_bf16.h>
 
@@ -161,17 +165,41 @@ verify_generic_kernel(VerifyArgs a) {
 
 // ---------------------------------------------------------------- planning --
 
+// Path choice.  TSD_VERIFY_PATH=generic|mma|tc forces a path where it
+// applies (used by the tests to check every path against the oracle).
+static int choose_path(const tsd_attn_desc& d, int M) {
+  const bool gqa_bf16 = d.dtype == TSD_BF16 && !d.v_aliases_k && d.dk == d.dv;
+  const bool mma_ok = gqa_bf16 && (d.dk == 64 || d.dk == 128);
+  const bool tc_ok = gqa_bf16 && d.dk == 128 && M >= kMmaMinRows && tc_path_available();
+  const char* force = getenv("TSD_VERIFY_PATH");
+  if (force != nullptr) {
+    if (strcmp(force, "generic") == 0) return kPathGeneric;
+    if (strcmp(force, "mma") == 0 && mma_ok) return kPathMma;
+    if (strcmp(force, "tc") == 0 && tc_ok) return kPathTc;
+  }
+  if (M < kMmaMinRows) return kPathGeneric;  // not a dense contraction
+  if (tc_ok) return kPathTc;
+  if (mma_ok) return kPathMma;
+  return kPathGeneric;
+}
+
 VerifyPlan plan_verify(const tsd_attn_desc& d) {
   // The split of the prefix depends only on per-request quantities (never on
   // B), so a request's result is bit-identical alone or inside any batch.
   VerifyPlan p{};
   const int M = d.R * (d.Hq / d.Hkv);
-  const bool mma = d.dtype == TSD_BF16 && !d.v_aliases_k && d.dk == d.dv &&
-                   (d.dk == 64 || d.dk == 128) && M >= kMmaMinRows;
+  p.path = choose_path(d, M);
   long ns;
-  if (mma) {
+  if (p.path == kPathTc) {
+    // packed rows on the MMA N dimension: at most 144 per CTA, multiple of 16
+    p.nrg = (int)ceil_div(M, 144);
+    p.rb = (int)ceil_div(ceil_div(M, p.nrg), 16) * 16;
+    ns = ceil_div(152L * 2, (long)d.Hkv * p.nrg);
+    long len = ceil_div(ceil_div(d.cap, ns), 128) * 128;  // whole 128-key tiles
+    if (len < 1024) len = 1024;  // a split's partial output costs about 130 keys of KV
+    p.split_len = (int)len;
+  } else if (p.path == kPathMma) {
     // one warp per 16 packed rows, at most 8 warps per CTA, balanced groups
-    p.path = kPathMma;
     const int nblk = (int)ceil_div(M, 16);
     p.nrg = (int)ceil_div(nblk, 8);
     p.rb = (int)ceil_div(nblk, p.nrg) * 16;
@@ -180,7 +208,6 @@ VerifyPlan plan_verify(const tsd_attn_desc& d) {
     len = ceil_div(len < 256 ? 256 : len, 64) * 64;       // whole 64-key tiles, >= 4 per split
     p.split_len = (int)len;
   } else {
-    p.path = kPathGeneric;
     p.rb = d.dk > 128 ? 2 : 8;
     p.nrg = (int)ceil_div(M, p.rb);
     ns = ceil_div(152L * 4, (long)d.Hkv * p.nrg);
@@ -254,8 +281,8 @@ extern "C" tsd_status tsd_tree_verify_attn(const tsd_attn_desc* d, const void* q
                                            const void* vtree, const uint64_t* mask, void* out,
                                            float* lse, void* ws, size_t ws_bytes, int32_t* err,
                                            tsd_stream_t stream) {
-  (void)err;
   if (!desc_ok(d)) return TSD_ERR_INVALID_ARG;
+  if ((((uintptr_t)err) & 3u) != 0) return TSD_ERR_INVALID_ARG;
   if (!ok_ptr(q) || !ok_ptr(kcache) || !ok_ptr(prefix_len) || !ok_ptr(ktree) || !ok_ptr(mask) ||
       !ok_ptr(out) || !ok_ptr(lse))
     return TSD_ERR_INVALID_ARG;
@@ -273,9 +300,12 @@ extern "C" tsd_status tsd_tree_verify_attn(const tsd_attn_desc* d, const void* q
   a.M = d->R * a.g; a.cap = d->cap;
   a.nsplit = p.nsplit; a.split_len = p.split_len; a.nrg = p.nrg;
   a.qscale = d->scale * 1.4426950408889634f;
+  a.err = err;
   const cudaStream_t st = (cudaStream_t)stream;
-  const bool launched = p.path == kPathMma ? launch_mma_path(*d, a, p, st)
-                                           : launch_generic_path(*d, a, p, st);
+  bool launched;
+  if (p.path == kPathTc) launched = launch_tc_path(*d, a, p, st);
+  else if (p.path == kPathMma) launched = launch_mma_path(*d, a, p, st);
+  else launched = launch_generic_path(*d, a, p, st);
   if (!launched) return TSD_ERR_UNSUPPORTED;
   return cuda_status();
 }

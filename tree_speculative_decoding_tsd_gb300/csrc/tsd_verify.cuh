@@ -31,7 +31,7 @@ struct VerifyArgs {
   float qscale;   // softmax scale * log2(e): scores are kept in the log2 domain
 };
 
-enum VerifyPathId { kPathGeneric = 0, kPathMma = 1 };
+enum VerifyPathId { kPathGeneric = 0, kPathMma = 1, kPathTc = 2 };
 
 struct VerifyPlan {
   int path;
@@ -48,6 +48,9 @@ constexpr int kMmaMinRows = 64;
 VerifyPlan plan_verify(const tsd_attn_desc& d);
 bool launch_mma_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPlan& p,
                      cudaStream_t st);
+bool launch_tc_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPlan& p,
+                    cudaStream_t st);
+bool tc_path_available();
 
 namespace {
 
