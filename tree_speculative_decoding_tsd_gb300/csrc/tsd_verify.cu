@@ -184,8 +184,6 @@ static int choose_path(const tsd_attn_desc& d, int M) {
 }
 
 VerifyPlan plan_verify(const tsd_attn_desc& d) {
-  // The split of the prefix depends only on per-request quantities (never on
-  // B), so a request's result is bit-identical alone or inside any batch.
   VerifyPlan p{};
   const int M = d.R * (d.Hq / d.Hkv);
   p.path = choose_path(d, M);
@@ -194,9 +192,17 @@ VerifyPlan plan_verify(const tsd_attn_desc& d) {
     // packed rows on the MMA N dimension: at most 144 per CTA, multiple of 16
     p.nrg = (int)ceil_div(M, 144);
     p.rb = (int)ceil_div(ceil_div(M, p.nrg), 16) * 16;
-    ns = ceil_div(152L * 2, (long)d.Hkv * p.nrg);
+    // Splits: about two waves of CTAs for the whole batch.  A split writes a
+    // partial output as large as ~130 keys of K/V, so splits stay >= 512 keys
+    // (>= 1024 once the batch alone fills the GPU) and <= 4096 keys.  The split
+    // depends on B: results are deterministic, but their rounding can differ
+    // between batch sizes.
+    const long units = (long)d.B * d.Hkv * p.nrg;
+    ns = ceil_div(152L * 2, units);
     long len = ceil_div(ceil_div(d.cap, ns), 128) * 128;  // whole 128-key tiles
-    if (len < 1024) len = 1024;  // a split's partial output costs about 130 keys of KV
+    const long lo = units >= 152 ? 1024 : 512;
+    if (len < lo) len = lo;
+    if (len > 4096) len = 4096;
     p.split_len = (int)len;
   } else if (p.path == kPathMma) {
     // one warp per 16 packed rows, at most 8 warps per CTA, balanced groups

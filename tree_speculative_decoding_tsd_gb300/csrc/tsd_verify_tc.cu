@@ -9,20 +9,26 @@
 //   O^T[d][n]   += V_tile^T . P^T   M = 128 (dv),  N = packed rows, K = 128 keys
 // Both accumulators live in tensor memory (fp32); S^T is double-buffered.
 //
-// Roles (320 threads): warps 0-7 softmax/epilogue (warpgroup w/4 owns half of
-// the columns, warp w%4 owns TMEM lanes 32(w%4)..+31, i.e. 32 keys of a tile
-// or 32 dims of O^T); warp 8 allocates TMEM and issues the MMAs (one thread);
-// warp 9 issues the TMA loads (one thread).  K/V tiles of 128 keys (64 KB per
-// stage, two stages) arrive by cp.async.bulk.tensor with 128-byte swizzle;
-// mbarriers order TMA -> MMA -> softmax -> MMA.
+// Roles (576 threads): warps 0-15 softmax/epilogue (warpgroup w/4 owns a
+// quarter of the columns, warp w%4 owns TMEM lanes 32(w%4)..+31, i.e. 32 keys
+// of a tile or 32 dims of O^T); warp 16 allocates TMEM and issues the MMAs
+// (one thread); warp 17 issues the TMA loads (one thread).  K and V tiles of 128 keys (32 KB
+// each) arrive by cp.async.bulk.tensor with 128-byte swizzle into two separate
+// two-stage rings: a K stage is refilled as soon as its S^T product is done, a V
+// stage as soon as its O^T product is done, so each load is issued about two
+// tiles ahead of its use.  mbarriers order TMA -> MMA -> softmax -> MMA.
 //
 // Softmax with keys on lanes: a thread holds one key's scores for all of its
 // columns, so a row's max and sum are cross-lane reductions.  The running max
-// m[n] is therefore lazy: it is recomputed exactly (warp reduce-scatter plus a
-// shared-memory pass) on the first tile and whenever a score exceeds it by more
-// than 8 in the log2 domain (probabilities stay <= 2^8, safe in bf16/fp32);
-// O^T columns and the partial sums are then rescaled by 2^(m_old - m_new).
-// Row sums accumulate per key lane and are reduced once, at the end.
+// m[n] is therefore lazy.  Each tile is first processed optimistically with
+// the current m (p = 2^min(x, 64), x = s*scale*log2e - m), adding p to the
+// per-lane partial sums and writing P^T.  If any x exceeded 8 (or on the first
+// tile) the warpgroup recomputes the tile exactly: column maxima by a warp
+// reduce-scatter plus a shared-memory pass, alpha = 2^(m_old - m_new), O^T
+// columns rescaled, and every partial sum replaced by (l - p_opt)*alpha + p_new
+// (the subtraction's rounding error is scaled by alpha, below 2^-24 of the new
+// sum).  Probabilities therefore stay <= 2^8, safe in bf16/fp32.  Row sums are
+// reduced across lanes once, at the end.
 //
 // Every mbarrier wait is bounded (about a second); a timeout sets
 // TSD_DEV_ERR_TIMEOUT in the error word, all roles stop, in-flight copies and
@@ -41,13 +47,16 @@ namespace {
 
 constexpr int kKeys = 128;          // keys per tile (MMA M of S^T)
 constexpr int kD = 128;             // head dim
-constexpr int kSoftWarps = 8;
+constexpr int kSoftWarps = 16;                  // 4 warpgroups, one quarter of the columns each
 constexpr int kThreadsTC = (kSoftWarps + 2) * 32;
-constexpr int kMmaWarp = 8, kTmaWarp = 9;
+constexpr int kMmaWarp = 16, kTmaWarp = 17;
 constexpr uint32_t kBox = kKeys * 128;          // one [128 rows][64 bf16] swizzled box: 16 KB
-constexpr uint32_t kStageBytes = 4 * kBox;      // K (2 boxes) + V (2 boxes)
-constexpr uint32_t kOffQ = 2 * kStageBytes;     // 128 KB
+constexpr uint32_t kTileBytes = 2 * kBox;       // one K or V tile: 32 KB
+constexpr uint32_t kOffK = 0;                   // K ring: 2 x 32 KB
+constexpr uint32_t kOffV = 2 * kTileBytes;      // V ring: 2 x 32 KB
+constexpr uint32_t kOffQ = 4 * kTileBytes;      // 128 KB
 constexpr float kOverflow = 8.0f;               // log2 headroom of the lazy max
+constexpr int kPrefetch = 3;                    // prefix tiles prefetched into L2 ahead
 constexpr long long kWaitCycles = 2000000000ll; // ~1 s at 2 GHz
 
 template <int N>
@@ -56,23 +65,25 @@ struct TcLayout {
   static constexpr uint32_t off_pt = kOffQ + ((q_bytes + 1023u) / 1024u) * 1024u;
   static constexpr uint32_t pt_blocks = (N + 63) / 64;
   static constexpr uint32_t off_misc = off_pt + pt_blocks * kBox;
-  static constexpr int NH = N / 2;                // columns per warpgroup
+  static constexpr int NH = N / 4;                // columns per warpgroup
   // misc area
   static constexpr uint32_t off_m = off_misc;                       // float[N]   running max
   static constexpr uint32_t off_alpha = off_m + 4 * N;              // float[N]   rescale factors
-  static constexpr uint32_t off_red = off_alpha + 4 * N;            // float[8][NH] per-warp partials
-  static constexpr uint32_t off_lsum = off_red + 4 * 8 * NH;        // float[N]   row sums
+  static constexpr uint32_t off_negm = off_alpha + 4 * N;             // float[N]   -m (0 if m = -inf)
+  static constexpr uint32_t off_red = off_negm + 4 * N;             // float[16][NH] per-warp partials
+  static constexpr uint32_t off_lsum = off_red + 4 * kSoftWarps * NH;  // float[N] row sums
   static constexpr uint32_t off_rmask = (off_lsum + 4 * N + 7) / 8 * 8;  // u64[N] tree masks
-  static constexpr uint32_t off_bar = off_rmask + 8 * N;            // mbarriers
-  static constexpr int nbar = 10;
+  static constexpr uint32_t off_ooff = off_rmask + 8 * N;           // i64[N] output offsets
+  static constexpr uint32_t off_bar = off_ooff + 8 * N;             // mbarriers
+  static constexpr int nbar = 13;
   static constexpr uint32_t off_flags = off_bar + 8 * nbar;          // tmem addr, abort flag
   static constexpr uint32_t total = off_flags + 16;
   static_assert(total + 1024 <= 232448, "shared memory budget");
 };
 
 // barrier indices
-enum { BAR_KV_FULL = 0, BAR_KV_EMPTY = 2, BAR_S_FULL = 4, BAR_P_FULL = 6, BAR_PV_DONE = 7,
-       BAR_FINAL = 8 };
+enum { BAR_K_FULL = 0, BAR_K_EMPTY = 2, BAR_V_FULL = 4, BAR_V_EMPTY = 6, BAR_S_FULL = 8,
+       BAR_P_FULL = 10, BAR_PV_DONE = 11, BAR_FINAL = 12 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -119,6 +130,17 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int
       : "memory");
 }
 
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(map),
+               "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
@@ -141,6 +163,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32: about 2 ulp,
+// results below 2^-126 flush to zero -- irrelevant for softmax weights)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 
@@ -153,6 +182,19 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
       : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const float (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])));
 }
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
   asm volatile(
@@ -274,36 +316,82 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
   const int rows_here = min(rows_per_cta, a.M - row_base);
 
   // ---------------------------------------------------------------- set-up
-  if (warp == kMmaWarp) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
-        sbase + L::off_flags));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
-  }
+  // The TMA thread initialises the barriers and starts the first loads at
+  // once, so they overlap the Q staging and the TMEM allocation.
+  auto ycoord = [&](int t) { return (b * a.Hkv + hk) * a.cap + k0 + t * kKeys; };
+  auto tma_k = [&](int t, int stage) {
+    const uint32_t dst = sbase + kOffK + stage * kTileBytes;
+    const uint32_t fb = bar(BAR_K_FULL + stage);
+    mbar_expect_tx(fb, kTileBytes);
+    if (t < n_pre) {
+      tma_2d(dst, &maps.k, 0, ycoord(t), fb);
+      tma_2d(dst + kBox, &maps.k, 64, ycoord(t), fb);
+    } else {
+      tma_3d(dst, &maps.kt, 0, hk, b * a.R, fb);
+      tma_3d(dst + kBox, &maps.kt, 64, hk, b * a.R, fb);
+    }
+  };
+  auto tma_v = [&](int t, int stage) {
+    const uint32_t dst = sbase + kOffV + stage * kTileBytes;
+    const uint32_t fb = bar(BAR_V_FULL + stage);
+    mbar_expect_tx(fb, kTileBytes);
+    if (t < n_pre) {
+      tma_2d(dst, &maps.v, 0, ycoord(t), fb);
+      tma_2d(dst + kBox, &maps.v, 64, ycoord(t), fb);
+    } else {
+      tma_3d(dst, &maps.vt, 0, hk, b * a.R, fb);
+      tma_3d(dst + kBox, &maps.vt, 64, hk, b * a.R, fb);
+    }
+  };
+  // L2 prefetch of a prefix tile a few tiles ahead of its smem load
+  auto prefetch = [&](int t) {
+    if (t < n_pre) {
+      tma_prefetch_2d(&maps.k, 0, ycoord(t));
+      tma_prefetch_2d(&maps.k, 64, ycoord(t));
+      tma_prefetch_2d(&maps.v, 0, ycoord(t));
+      tma_prefetch_2d(&maps.v, 64, ycoord(t));
+    }
+  };
   if (tid == kTmaWarp * 32) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(BAR_KV_FULL + s), 1);
-      mbar_init(bar(BAR_KV_EMPTY + s), 1);
-      mbar_init(bar(BAR_S_FULL + s), 1);
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(bar(BAR_K_FULL + s2), 1);
+      mbar_init(bar(BAR_K_EMPTY + s2), 1);
+      mbar_init(bar(BAR_V_FULL + s2), 1);
+      mbar_init(bar(BAR_V_EMPTY + s2), 1);
+      mbar_init(bar(BAR_S_FULL + s2), 1);
     }
     mbar_init(bar(BAR_P_FULL), kSoftWarps);
     mbar_init(bar(BAR_PV_DONE), 1);
     mbar_init(bar(BAR_FINAL), 1);
     flags[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    tma_k(0, 0);
+    tma_v(0, 0);
+    if (ntiles > 1) tma_k(1, 1);
+    for (int t = 2; t < 2 + kPrefetch; ++t) prefetch(t);
   }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
+        sbase + L::off_flags));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  float* negm = (float*)(smem + L::off_negm);
+  long long* ooff = (long long*)(smem + L::off_ooff);
   if (warp < kSoftWarps) {
-    // Q tile (K-major, 128-byte swizzle: two boxes of [N][64]) and tree masks
+    // Q tile (K-major, 128-byte swizzle: two boxes of [N][64]) by cp.async
     for (int idx = tid; idx < N * 16; idx += kSoftWarps * 32) {
       const int n = idx >> 4, c = idx & 15;
-      const int p = row_base + n;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (n < rows_here) {
+      const bool valid = n < rows_here;
+      const __nv_bfloat16* src = (const __nv_bfloat16*)a.q;
+      if (valid) {
+        const int p = row_base + n;
         const int tr = p / a.g, qh = hk * a.g + p % a.g;
-        val = *(const uint4*)((const __nv_bfloat16*)a.q + (((long)b * a.R + tr) * a.Hq + qh) * kD + c * 8);
+        src += (((long)b * a.R + tr) * a.Hq + qh) * kD + c * 8;
       }
-      const uint32_t off = kOffQ + (c >> 3) * (N * 128u) + n * 128u + (((c & 7) ^ (n & 7)) << 4);
-      *(uint4*)(smem + off) = val;
+      cp_async16(sbase + kOffQ + (c >> 3) * (N * 128u) + n * 128u + (((c & 7) ^ (n & 7)) << 4),
+                 src, valid);
     }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
     for (int n = tid; n < N; n += kSoftWarps * 32) {
       uint64_t mk = 0ull;
       if (n < rows_here) {
@@ -312,7 +400,9 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
       }
       rmask[n] = mk;
       m_run[n] = -INFINITY;
+      negm[n] = 0.f;
     }
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
   fence_before();
@@ -325,35 +415,32 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
   // ------------------------------------------------------------------ TMA
   if (warp == kTmaWarp) {
     if (lane == 0) {
-      int issued[2] = {0, 0};
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t & 1;
-        if (t >= 2 && !mbar_wait(bar(BAR_KV_EMPTY + st), ((t >> 1) - 1) & 1)) {
-          flags[1] = 1;
-          break;
+      // Loads in the order their stages free up: K_t after S^T_{t-2}, then
+      // V_{t-1} after O^T_{t-3} (the MMA completes in issue order).
+      int nk = ntiles > 1 ? 2 : 1, nv = 1;
+      for (int t = 2; t <= ntiles && !flags[1]; ++t) {
+        if (t < ntiles) {
+          if (!mbar_wait(bar(BAR_K_EMPTY + (t & 1)), ((t - 2) >> 1) & 1)) { flags[1] = 1; break; }
+          tma_k(t, t & 1);
+          prefetch(t + kPrefetch);
+          ++nk;
         }
-        if (flags[1]) break;
-        const uint32_t dst = sbase + st * kStageBytes;
-        const uint32_t fb = bar(BAR_KV_FULL + st);
-        mbar_expect_tx(fb, kStageBytes);
-        if (t < n_pre) {
-          const int y = (b * a.Hkv + hk) * a.cap + k0 + t * kKeys;
-          tma_2d(dst, &maps.k, 0, y, fb);
-          tma_2d(dst + kBox, &maps.k, 64, y, fb);
-          tma_2d(dst + 2 * kBox, &maps.v, 0, y, fb);
-          tma_2d(dst + 3 * kBox, &maps.v, 64, y, fb);
-        } else {
-          const int z = b * a.R;
-          tma_3d(dst, &maps.kt, 0, hk, z, fb);
-          tma_3d(dst + kBox, &maps.kt, 64, hk, z, fb);
-          tma_3d(dst + 2 * kBox, &maps.vt, 0, hk, z, fb);
-          tma_3d(dst + 3 * kBox, &maps.vt, 64, hk, z, fb);
+        const int tv = t - 1;
+        if (tv < ntiles) {
+          if (tv >= 2 && !mbar_wait(bar(BAR_V_EMPTY + (tv & 1)), ((tv - 2) >> 1) & 1)) {
+            flags[1] = 1;
+            break;
+          }
+          tma_v(tv, tv & 1);
+          ++nv;
         }
-        ++issued[st];
       }
       // no copy may still be in flight when the CTA leaves
-      for (int st = 0; st < 2; ++st)
-        if (issued[st] > 0) mbar_wait(bar(BAR_KV_FULL + st), (issued[st] - 1) & 1);
+      for (int st = 0; st < 2; ++st) {
+        const int ck = (nk - st + 1) / 2, cv = (nv - st + 1) / 2;  // loads into stage st
+        if (ck > 0) mbar_wait(bar(BAR_K_FULL + st), (ck - 1) & 1);
+        if (cv > 0) mbar_wait(bar(BAR_V_FULL + st), (cv - 1) & 1);
+      }
     }
   }
 
@@ -366,9 +453,9 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
       const uint32_t qa = sbase + kOffQ, pta = sbase + L::off_pt;
       auto issue_qk = [&](int t) -> bool {
         const int st = t & 1;
-        if (!mbar_wait(bar(BAR_KV_FULL + st), (t >> 1) & 1)) return false;
+        if (!mbar_wait(bar(BAR_K_FULL + st), (t >> 1) & 1)) return false;
         fence_after();
-        const uint32_t kb = sbase + st * kStageBytes;
+        const uint32_t kb = sbase + kOffK + st * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint64_t ad = smem_desc(kb + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
@@ -376,14 +463,16 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
           mma_f16(tm_s[st], ad, bd, idesc_qk, kk > 0);
         }
         mma_commit(bar(BAR_S_FULL + st));
+        mma_commit(bar(BAR_K_EMPTY + st));
         return true;
       };
-      bool ok = ntiles == 0 || issue_qk(0);
+      bool ok = issue_qk(0);
       for (int t = 0; ok && t < ntiles; ++t) {
         if (t + 1 < ntiles && !issue_qk(t + 1)) { ok = false; break; }
         if (!mbar_wait(bar(BAR_P_FULL), t & 1) || flags[1]) { ok = false; break; }
+        if (!mbar_wait(bar(BAR_V_FULL + (t & 1)), (t >> 1) & 1)) { ok = false; break; }
         fence_after();
-        const uint32_t vb = sbase + (t & 1) * kStageBytes + 2 * kBox;
+        const uint32_t vb = sbase + kOffV + (t & 1) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
           const uint64_t ad = smem_desc(vb + kk * 2048, kBox, 1024);
@@ -391,10 +480,11 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
           mma_f16(tm_o, ad, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(BAR_PV_DONE));
-        mma_commit(bar(BAR_KV_EMPTY + (t & 1)));
+        mma_commit(bar(BAR_V_EMPTY + (t & 1)));
       }
       if (!ok) flags[1] = 1;
-      // every MMA issued so far has completed once this barrier flips
+      // every MMA issued so far has completed once this commit lands: wait for
+      // it before the TMEM is released
       mma_commit(bar(BAR_FINAL));
       mbar_wait(bar(BAR_FINAL), 0);
     }
@@ -407,9 +497,10 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
     const int key = q * 32 + lane;           // TMEM lane = key of the tile / dim of O^T
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float c = a.qscale;
-    // the warpgroup's columns are handled in two halves of H0 and H1 columns
-    constexpr int H0 = ((NH / 2 + 7) / 8) * 8, H1 = NH - H0;
-    float l[NH];
+    constexpr int NCH = NH / 4;              // chunks of 4 columns (one tcgen05.ld.x4 each)
+    constexpr int GRP = 6;                   // chunks loaded per tcgen05.wait::ld
+    float l[NH];                             // this key lane's partial row sums
+    uint32_t pp[NH / 2];                     // this tile's probabilities, packed bf16x2
 #pragma unroll
     for (int n = 0; n < NH; ++n) l[n] = 0.f;
     bool failed = false;
@@ -421,49 +512,72 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
       fence_after();
       const bool is_tree = t >= n_pre;
       const int nvalid = is_tree ? a.R : min(kKeys, k1 - (k0 + t * kKeys));
-      // scores of this key for columns [h0, h0 + H) with the masks applied
-      auto load = [&](float* x, int h0, int H) {
-        for (int j = 0; j < H / 8; ++j) {
-          float v[8];
-          tmem_ld8(tm_s[st] + lane_off + (uint32_t)(c0 + h0 + 8 * j), v);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) x[8 * j + i] = v[i];
-        }
-        tmem_wait_ld();
+      const uint32_t srow = tm_s[st] + lane_off + (uint32_t)c0;
+      // masked scores of chunk j (columns c0 + 4j .. +3) of this key
+      auto masked = [&](float (&v)[4], int j) {
         if (key >= nvalid) {
-          for (int n = 0; n < H; ++n) x[n] = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[i] = -INFINITY;
         } else if (is_tree && key > 0) {
-          for (int n = 0; n < H; ++n)
-            if (!((rmask[c0 + h0 + n] >> (key - 1)) & 1ull)) x[n] = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (!((rmask[c0 + 4 * j + i] >> (key - 1)) & 1ull)) v[i] = -INFINITY;
         }
       };
-      // pass A: does any score pass the lazy max by more than the headroom?
-      bool over = (t == 0);
+      // x = s*c - m (log2 domain), p = 2^min(x, 64); returns max x
+      auto probs = [&](float (&v)[4], int j) {
+        const float4 nm = *(const float4*)(negm + c0 + 4 * j);
+        const float x0 = fmaf(v[0], c, nm.x), x1 = fmaf(v[1], c, nm.y);
+        const float x2 = fmaf(v[2], c, nm.z), x3 = fmaf(v[3], c, nm.w);
+        v[0] = ex2(fminf(x0, 64.f));
+        v[1] = ex2(fminf(x1, 64.f));
+        v[2] = ex2(fminf(x2, 64.f));
+        v[3] = ex2(fminf(x3, 64.f));
+        return fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+      };
+      auto load1 = [&](float (&v)[4], int j) {
+        tmem_ld4(srow + 4u * j, v);
+        tmem_wait_ld();
+        masked(v, j);
+      };
+
+      // optimistic pass with the current running max
+      float xmax = -INFINITY;
       if (ok) {
-        float x[H0];
-        load(x, 0, H0);
 #pragma unroll
-        for (int n = 0; n < H0; ++n) {
-          const float mu = m_run[c0 + n];
-          over |= fmaf(x[n], c, -(mu == -INFINITY ? 0.f : mu)) > kOverflow;
-        }
-        load(x, H0, H1);
+        for (int j0 = 0; j0 < NCH; j0 += GRP) {
+          float v[GRP][4];
 #pragma unroll
-        for (int n = 0; n < H1; ++n) {
-          const float mu = m_run[c0 + H0 + n];
-          over |= fmaf(x[n], c, -(mu == -INFINITY ? 0.f : mu)) > kOverflow;
+          for (int u = 0; u < GRP; ++u)
+            if (j0 + u < NCH) tmem_ld4(srow + 4u * (j0 + u), v[u]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < GRP; ++u) {
+            const int j = j0 + u;
+            if (j >= NCH) break;
+            masked(v[u], j);
+            xmax = fmaxf(xmax, probs(v[u], j));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) l[4 * j + i] += v[u][i];
+            pp[2 * j] = pack_bf16x2(v[u][0], v[u][1]);
+            pp[2 * j + 1] = pack_bf16x2(v[u][2], v[u][3]);
+          }
         }
       }
-      const bool stop = wg_bar_or(wg, !ok || failed || flags[1] != 0);
-      if (stop) { failed = true; break; }
-      const bool any_over = wg_bar_or(wg, over);
-      if (any_over) {
+      // one barrier in the common case; the rare path takes a second one
+      const bool local_stop = !ok || failed || flags[1] != 0;
+      bool slow = false;
+      if (wg_bar_or(wg, local_stop || t == 0 || xmax > kOverflow)) {
+        if (wg_bar_or(wg, local_stop)) { failed = true; break; }
+        slow = true;
         // exact column maxima of this tile, then the new running max
-        float x[H0];
-        load(x, 0, H0);
-        warp_columns<H0, true>(x, red + warp * NH, lane);
-        load(x, H0, H1);
-        warp_columns<H1, true>(x, red + warp * NH + H0, lane);
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          float v[4];
+          load1(v, j);
+          const float r = warp_reduce_scatter<4, true>(v, lane);
+          if (lane < 4) red[warp * NH + 4 * j + lane] = r;
+        }
         wg_bar(wg);
         for (int n = tid & 127; n < NH; n += 128) {
           float mx = -INFINITY;
@@ -471,61 +585,65 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
           for (int w = 0; w < 4; ++w) mx = fmaxf(mx, red[(wg * 4 + w) * NH + n]);
           const float m_old = m_run[c0 + n];
           const float m_new = fmaxf(m_old, mx * c);
-          alpha[c0 + n] = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
+          alpha[c0 + n] = (m_old == -INFINITY) ? 0.f : ex2(m_old - m_new);
           m_run[c0 + n] = m_new;
         }
         wg_bar(wg);
+        // take the optimistic probabilities back out (recomputed bit-identically)
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          float v[4];
+          load1(v, j);
+          probs(v, j);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) l[4 * j + i] -= v[i];
+        }
+        wg_bar(wg);
+        for (int n = tid & 127; n < NH; n += 128) {
+          const float mu = m_run[c0 + n];
+          negm[c0 + n] = mu == -INFINITY ? 0.f : -mu;
+        }
+        wg_bar(wg);
+        // exact probabilities with the new max; old sums rescaled by alpha
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          float v[4];
+          load1(v, j);
+          probs(v, j);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) l[4 * j + i] = fmaf(l[4 * j + i], alpha[c0 + 4 * j + i], v[i]);
+          pp[2 * j] = pack_bf16x2(v[0], v[1]);
+          pp[2 * j + 1] = pack_bf16x2(v[2], v[3]);
+        }
       }
-      // PV of the previous tile must be done before O^T or P^T are touched
+      // P^T is single-buffered: the previous tile's O^T product must be done
       if (t > 0 && !__all_sync(kFull, mbar_wait(bar(BAR_PV_DONE), (t - 1) & 1))) failed = true;
       fence_after();
-      if (any_over && t > 0 && !failed) {
+      if (slow && t > 0 && !failed) {
 #pragma unroll
-        for (int n = 0; n < NH; ++n) l[n] *= alpha[c0 + n];
-        for (int j = 0; j < NH / 8; ++j) {
-          float v[8];
-          tmem_ld8(tm_o + lane_off + (uint32_t)(c0 + 8 * j), v);
+        for (int j = 0; j < NCH; ++j) {
+          float v[4];
+          tmem_ld4(tm_o + lane_off + (uint32_t)(c0 + 4 * j), v);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] *= alpha[c0 + 8 * j + i];
-          tmem_st8(tm_o + lane_off + (uint32_t)(c0 + 8 * j), v);
+          for (int i = 0; i < 4; ++i) v[i] *= alpha[c0 + 4 * j + i];
+          tmem_st4(tm_o + lane_off + (uint32_t)(c0 + 4 * j), v);
         }
         tmem_wait_st();
       }
-      // pass B: probabilities, partial row sums, P^T row of this key
-      // (MN-major, 128-byte swizzle, blocks of 64 columns)
-      auto emit = [&](float* x, int h0, int H) {
-        for (int n = 0; n < H; ++n) {
-          const float mu = m_run[c0 + h0 + n];
-          x[n] = exp2f(fmaf(x[n], c, -(mu == -INFINITY ? 0.f : mu)));
-        }
-        for (int j = 0; j < H / 8; ++j) {
-          const int n0 = c0 + h0 + 8 * j;
-          uint4 pk;
-          pk.x = pack_bf16x2(x[8 * j], x[8 * j + 1]);
-          pk.y = pack_bf16x2(x[8 * j + 2], x[8 * j + 3]);
-          pk.z = pack_bf16x2(x[8 * j + 4], x[8 * j + 5]);
-          pk.w = pack_bf16x2(x[8 * j + 6], x[8 * j + 7]);
-          const uint32_t off = L::off_pt + (n0 >> 6) * kBox + key * 128u +
-                               ((((n0 & 63) >> 3) ^ (key & 7)) << 4);
-          *(uint4*)(smem + off) = pk;
-        }
-      };
-      {
-        float x[H0];
-        load(x, 0, H0);
-        emit(x, 0, H0);
+      // P^T row of this key (MN-major, 128-byte swizzle, blocks of 64 columns)
 #pragma unroll
-        for (int n = 0; n < H0; ++n) l[n] += x[n];
-        load(x, H0, H1);
-        emit(x, H0, H1);
-#pragma unroll
-        for (int n = 0; n < H1; ++n) l[H0 + n] += x[n];
+      for (int j = 0; j < NCH; ++j) {
+        const int n0 = c0 + 4 * j;
+        const uint32_t off = L::off_pt + (n0 >> 6) * kBox + key * 128u +
+                             ((((n0 & 63) >> 3) ^ (key & 7)) << 4) + ((n0 & 4) << 1);
+        *(uint2*)(smem + off) = make_uint2(pp[2 * j], pp[2 * j + 1]);
       }
-      // V rows of keys past the range may hold anything: zero them
-      if (key >= nvalid) {
-        if (!mbar_wait(bar(BAR_KV_FULL + st), (t >> 1) & 1)) failed = true;
-        uint8_t* vrow = smem + st * kStageBytes + 2 * kBox + key * 128u;
+      // V rows of keys past the range may hold anything: zero them (the
+      // warpgroup of the first columns does it)
+      if (wg == 0 && key >= nvalid) {
+        if (!mbar_wait(bar(BAR_V_FULL + st), (t >> 1) & 1)) failed = true;
+        uint8_t* vrow = smem + kOffV + st * kTileBytes + key * 128u;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           *(uint4*)(vrow + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
@@ -544,38 +662,52 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
     fence_after();
     const bool stop = wg_bar_or(wg, !ok || flags[1] != 0);
     if (!stop) {
-      warp_columns<H0, false>(l, red + warp * NH, lane);
-      warp_columns<H1, false>(l + H0, red + warp * NH + H0, lane);
-      wg_bar(wg);
-      for (int n = tid & 127; n < NH; n += 128) {
-        float sum = 0.f;
+      // row sums across the 128 key lanes
 #pragma unroll
-        for (int w = 0; w < 4; ++w) sum += red[(wg * 4 + w) * NH + n];
-        lsum[c0 + n] = sum;
+      for (int j = 0; j < NCH; ++j) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = l[4 * j + i];
+        const float r = warp_reduce_scatter<4, false>(v, lane);
+        if (lane < 4) red[warp * NH + 4 * j + lane] = r;
+      }
+      wg_bar(wg);
+      // per column: 1/l into alpha[], destination offset, log-sum-exp
+      for (int n = tid & 127; n < NH; n += 128) {
+        const int col = c0 + n;
+        float ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) ls += red[(wg * 4 + w) * NH + n];
+        alpha[col] = 1.f / ls;
+        if (col < rows_here) {
+          const int p = row_base + col;
+          const int tr = p / a.g, qh = hk * a.g + p % a.g;
+          const float lse2 = m_run[col] + log2f(ls);
+          if (a.nsplit == 1) {
+            const long orow = ((long)b * a.R + tr) * a.Hq + qh;
+            ooff[col] = orow * kD;
+            a.lse[orow] = lse2 * 0.69314718055994531f;
+          } else {
+            const long prow = (((long)b * a.Hq + qh) * a.R + tr) * a.nsplit + sp;
+            ooff[col] = prow * kD;
+            a.ws_lse[prow] = lse2;
+          }
+        }
       }
       wg_bar(wg);
       const int d = key;  // O^T lane = output dim
-      for (int j = 0; j < NH / 8; ++j) {
-        float v[8];
-        tmem_ld8(tm_o + lane_off + (uint32_t)(c0 + 8 * j), v);
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        float v[4];
+        tmem_ld4(tm_o + lane_off + (uint32_t)(c0 + 4 * j), v);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int n = c0 + 8 * j + i;
-          if (n >= rows_here) continue;
-          const int p = row_base + n;
-          const int tr = p / a.g, qh = hk * a.g + p % a.g;
-          const float ls = lsum[n];
-          const float res = v[i] / ls;
-          if (a.nsplit == 1) {
-            const long orow = ((long)b * a.R + tr) * a.Hq + qh;
-            ((__nv_bfloat16*)a.out)[orow * kD + d] = __float2bfloat16_rn(res);
-            if (d == 0) a.lse[orow] = (m_run[n] + log2f(ls)) * 0.69314718055994531f;
-          } else {
-            const long prow = (((long)b * a.Hq + qh) * a.R + tr) * a.nsplit + sp;
-            a.ws_o[prow * kD + d] = res;
-            if (d == 0) a.ws_lse[prow] = m_run[n] + log2f(ls);
-          }
+        for (int i = 0; i < 4; ++i) {
+          const int col = c0 + 4 * j + i;
+          if (col >= rows_here) break;
+          const float res = v[i] * alpha[col];
+          if (a.nsplit == 1) ((__nv_bfloat16*)a.out)[ooff[col] + d] = __float2bfloat16_rn(res);
+          else a.ws_o[ooff[col] + d] = res;
         }
       }
     }
