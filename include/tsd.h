@@ -196,6 +196,31 @@ tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, int V,
                            int32_t* err, tsd_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * tsd_accept_walk_static
+ *
+ * No counterpart on the pages: this is tsd_accept_walk for callers that cannot
+ * allocate device memory -- code that is handed only its input and output
+ * buffers, such as a custom operator inside another framework whose memory
+ * planner owns the device heap, or a serving loop that allows no allocation
+ * after start-up.  Arguments and results are those of tsd_accept_walk, minus
+ * the workspace.  The scratch lives in a fixed 1 MiB array inside the library
+ * (each GPU that loads the library holds it until the process exits); a call
+ * whose tsd_accept_walk_workspace_size(B, D, V) exceeds 1 MiB returns
+ * TSD_ERR_UNSUPPORTED.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress), so make that first call before any stream
+ * capture.  Calls that overlap on the GPU (on different streams) share the
+ * array and race.  Nothing in the array needs to start at zero.  The call
+ * allocates and frees nothing.
+ * -------------------------------------------------------------------------- */
+tsd_status tsd_accept_walk_static(const float* logits, int B, int D, int S, int V,
+                                  const int32_t* token, const int32_t* parent,
+                                  const uint64_t* mask, const uint8_t* is_leaf,
+                                  int32_t* tgt, int32_t* accept_len,
+                                  int32_t* accept_rows, int32_t* bonus,
+                                  int32_t* chain_id, int32_t* err,
+                                  tsd_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * tsd_commit_path
  *
  * Accepted-path commit (V4 review, "Secret weapon" and toy step 6): only the

@@ -43,7 +43,8 @@ TSD_BF16 = 1
 # every symbol the header declares
 EXPORTED = ("tsd_status_string", "tsd_version", "tsd_tree_build_workspace_size",
             "tsd_tree_build", "tsd_verify_workspace_size", "tsd_tree_verify_attn",
-            "tsd_accept_walk_workspace_size", "tsd_accept_walk", "tsd_commit_path")
+            "tsd_accept_walk_workspace_size", "tsd_accept_walk", "tsd_accept_walk_static",
+            "tsd_commit_path")
 
 
 class TsdError(RuntimeError):
@@ -80,6 +81,8 @@ def _load():
     lib.tsd_accept_walk_workspace_size.restype = Z
     lib.tsd_accept_walk.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, P, P, Z, P, P]
     lib.tsd_accept_walk.restype = I
+    lib.tsd_accept_walk_static.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P]
+    lib.tsd_accept_walk_static.restype = I
     lib.tsd_commit_path.argtypes = [ctypes.POINTER(tsd_attn_desc), I, P, P, P, P, P, P, P, P, P]
     lib.tsd_commit_path.restype = I
     return lib
@@ -170,6 +173,16 @@ def tsd_accept_walk(logits, S, token, parent, mask, is_leaf, tgt, accept_len, ac
         _ptr(logits), B, R - 1, S, V, _ptr(token), _ptr(parent), _ptr(mask), _ptr(is_leaf),
         _ptr(tgt), _ptr(accept_len), _ptr(accept_rows), _ptr(bonus), _ptr(chain_id), _ptr(ws),
         _nbytes(ws), _ptr(err), _stream(stream)))
+
+
+def tsd_accept_walk_static(logits, S, token, parent, mask, is_leaf, tgt, accept_len, accept_rows,
+                           bonus, chain_id, err=None, stream=None):
+    """tsd_accept_walk without a workspace (fixed in-library scratch; see tsd.h)."""
+    B, R, V = logits.shape
+    _check("tsd_accept_walk_static", lib.tsd_accept_walk_static(
+        _ptr(logits), B, R - 1, S, V, _ptr(token), _ptr(parent), _ptr(mask), _ptr(is_leaf),
+        _ptr(tgt), _ptr(accept_len), _ptr(accept_rows), _ptr(bonus), _ptr(chain_id), _ptr(err),
+        _stream(stream)))
 
 
 def tsd_commit_path(desc, S, ktree, vtree, accept_rows, accept_len, kcache, vcache, prefix_len,

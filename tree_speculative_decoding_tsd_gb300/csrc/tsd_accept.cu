@@ -19,6 +19,8 @@
 #include "tsd_host.h"
 #include "tsd_scan.cuh"
 
+#include <mutex>
+
 namespace tsd {
 namespace {
 
@@ -149,6 +151,76 @@ extern "C" tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, 
   const long rows = (long)B * R;
   const ScanGeom g = scan_geometry(rows, V, 1);
   uint64_t* part = (uint64_t*)ws;
+  vocab_scan_kernel<true><<<(unsigned)(rows * g.nchunk), kScanThreads, 0, st>>>(
+      logits, V, 1, g.nchunk, g.chunk_len, part);
+  accept_walk_kernel<<<B, 32, 0, st>>>(part, R, S, g.nchunk, token, parent, mask, is_leaf, tgt,
+                                       accept_len, accept_rows, bonus, chain_id, err);
+  return cuda_status();
+}
+
+// ---------------------------------------------------------------------------
+// tsd_accept_walk_static: the same walk for callers that cannot allocate.
+//
+// Some callers are only ever handed their input and output buffers: a custom
+// operator running inside another framework whose memory planner owns the
+// device heap, or a serving loop that forbids any allocation after start-up.
+// They cannot call cudaMalloc and have no workspace to pass.  This entry point
+// keeps the per-chunk argmax candidates in a fixed array that is part of the
+// library image instead (every GPU that loads the library holds it until the
+// process exits), and allocates nothing itself.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr size_t kWalkStaticScratchBytes = size_t(1) << 20;  // 1 MiB
+static __device__ __align__(256) uint64_t g_walk_static_scratch[kWalkStaticScratchBytes / 8];
+
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress once per device (the first call on a device does it).
+uint64_t* walk_static_scratch() {
+  constexpr int kMaxDevices = 64;
+  static uint64_t* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_walk_static_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = (uint64_t*)p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" tsd_status tsd_accept_walk_static(const float* logits, int B, int D, int S, int V,
+                                             const int32_t* token, const int32_t* parent,
+                                             const uint64_t* mask, const uint8_t* is_leaf,
+                                             int32_t* tgt, int32_t* accept_len,
+                                             int32_t* accept_rows, int32_t* bonus,
+                                             int32_t* chain_id, int32_t* err,
+                                             tsd_stream_t stream) {
+  if (B < 1 || D < 1 || D > kMaxR - 1 || S < 1 || S > 16 || V < 1 || V > (1 << 30))
+    return TSD_ERR_INVALID_ARG;
+  if ((long)B * (D + 1) > (1l << 24)) return TSD_ERR_INVALID_ARG;
+  if (!ok_ptr(logits) || !ok_ptr(token) || !ok_ptr(parent) || !ok_ptr(mask) ||
+      !ok_ptr(is_leaf) || !ok_opt_ptr(tgt) || !ok_ptr(accept_len) || !ok_ptr(accept_rows) ||
+      !ok_ptr(bonus) || !ok_ptr(chain_id) || !ok_opt_ptr(err))
+    return TSD_ERR_INVALID_ARG;
+  // the fixed scratch bounds the problem size
+  if (tsd_accept_walk_workspace_size(B, D, V) > kWalkStaticScratchBytes) return TSD_ERR_UNSUPPORTED;
+  uint64_t* part = walk_static_scratch();
+  if (part == nullptr) return TSD_ERR_CUDA;
+
+  // Every scratch slot the walk reads is written by the scan of the same call,
+  // so nothing needs clearing.  Calls that overlap on the GPU share the array
+  // and race.
+  const cudaStream_t st = (cudaStream_t)stream;
+  const int R = D + 1;
+  const long rows = (long)B * R;
+  const ScanGeom g = scan_geometry(rows, V, 1);
   vocab_scan_kernel<true><<<(unsigned)(rows * g.nchunk), kScanThreads, 0, st>>>(
       logits, V, 1, g.nchunk, g.chunk_len, part);
   accept_walk_kernel<<<B, 32, 0, st>>>(part, R, S, g.nchunk, token, parent, mask, is_leaf, tgt,
