@@ -26,7 +26,9 @@ namespace {
 
 constexpr int kMaxR = 65;
 
-__global__ void __launch_bounds__(32)
+constexpr int kWalkWarps = 8;
+
+__global__ void __launch_bounds__(32 * kWalkWarps)
 accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
                    const int32_t* __restrict__ token, const int32_t* __restrict__ parent,
                    const uint64_t* __restrict__ mask, const uint8_t* __restrict__ is_leaf,
@@ -37,37 +39,40 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
   __shared__ uint64_t s_mask[kMaxR];
   __shared__ uint8_t s_leaf[kMaxR];
   const int b = blockIdx.x;
-  const int lane = threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long o = (long)b * R;
 
-  // tgt[r]: the largest of the row's chunk maxima (lanes split the chunks)
-  for (int r0 = 0; r0 < R; r0 += 4) {
-    uint64_t best[4];
+  // tgt[r]: the largest of the row's chunk maxima.  Warp w takes rows w, w+8,
+  // ...; its lanes split the (at most 256) chunks and load them all at once.
+  for (int r = warp; r < R; r += kWalkWarps) {
+    const uint64_t* src = part + (o + r) * nchunk;
+    uint64_t c[kScanMaxCand / 32];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      best[u] = 0ull;
-      if (r0 + u < R) {
-        const uint64_t* src = part + (o + r0 + u) * nchunk;
-        for (int c = lane; c < nchunk; c += 32) best[u] = src[c] > best[u] ? src[c] : best[u];
-      }
+    for (int j = 0; j < kScanMaxCand / 32; ++j) {
+      const int i = lane + 32 * j;
+      c[j] = i < nchunk ? src[i] : 0ull;
     }
+    uint64_t best = 0ull;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint64_t m = warp_max_u64(best[u]);
-      if (lane == 0 && r0 + u < R) {
-        const int32_t t = (int32_t)cand_id(m);
-        s_tgt[r0 + u] = t;
-        if (tgt_out != nullptr) tgt_out[o + r0 + u] = t;
-      }
+    for (int j = 0; j < kScanMaxCand / 32; ++j) best = c[j] > best ? c[j] : best;
+    best = warp_max_u64(best);
+    if (lane == 0) {
+      const int32_t t = (int32_t)cand_id(best);
+      s_tgt[r] = t;
+      if (tgt_out != nullptr) tgt_out[o + r] = t;
     }
   }
-  bool bad = false;
-  for (int r = lane; r < R; r += 32) {
+  for (int r = threadIdx.x; r < R; r += 32 * kWalkWarps) {
     s_tok[r] = token[o + r];
-    const int32_t p = parent[o + r];
-    s_par[r] = p;
+    s_par[r] = parent[o + r];
     s_mask[r] = mask[o + r];
     s_leaf[r] = is_leaf[o + r];
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  bool bad = false;
+  for (int r = lane; r < R; r += 32) {
+    const int32_t p = s_par[r];
     if (r > 0 && (p < 0 || p >= r)) bad = true;
   }
   bad = __any_sync(kFull, bad);
@@ -153,7 +158,7 @@ extern "C" tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, 
   uint64_t* part = (uint64_t*)ws;
   vocab_scan_kernel<true><<<(unsigned)(rows * g.nchunk), kScanThreads, 0, st>>>(
       logits, V, 1, g.nchunk, g.chunk_len, part);
-  accept_walk_kernel<<<B, 32, 0, st>>>(part, R, S, g.nchunk, token, parent, mask, is_leaf, tgt,
+  accept_walk_kernel<<<B, 32 * kWalkWarps, 0, st>>>(part, R, S, g.nchunk, token, parent, mask, is_leaf, tgt,
                                        accept_len, accept_rows, bonus, chain_id, err);
   return cuda_status();
 }
@@ -223,7 +228,7 @@ extern "C" tsd_status tsd_accept_walk_static(const float* logits, int B, int D, 
   const ScanGeom g = scan_geometry(rows, V, 1);
   vocab_scan_kernel<true><<<(unsigned)(rows * g.nchunk), kScanThreads, 0, st>>>(
       logits, V, 1, g.nchunk, g.chunk_len, part);
-  accept_walk_kernel<<<B, 32, 0, st>>>(part, R, S, g.nchunk, token, parent, mask, is_leaf, tgt,
+  accept_walk_kernel<<<B, 32 * kWalkWarps, 0, st>>>(part, R, S, g.nchunk, token, parent, mask, is_leaf, tgt,
                                        accept_len, accept_rows, bonus, chain_id, err);
   return cuda_status();
 }

@@ -161,13 +161,27 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
       hi = fmaxf(hi, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
     }
     if (__any_sync(kFull, hi >= thr_v)) {
+      // only elements at or above the threshold value are offered: one warp
+      // round per pending element of the busiest lane, per float4
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
+        const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+        unsigned pend = 0;
+        if (have[u]) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) pend |= (e[i] >= thr_v) ? (1u << i) : 0u;
+        }
         const uint32_t i0 = (uint32_t)(a0 + 4 * (v0 + u * kScanThreads + lane));
-        warp_list_offer(entry, thr, have[u] ? make_cand(f[u].x, i0) : 0ull, k, kmask, lane);
-        warp_list_offer(entry, thr, have[u] ? make_cand(f[u].y, i0 + 1) : 0ull, k, kmask, lane);
-        warp_list_offer(entry, thr, have[u] ? make_cand(f[u].z, i0 + 2) : 0ull, k, kmask, lane);
-        warp_list_offer(entry, thr, have[u] ? make_cand(f[u].w, i0 + 3) : 0ull, k, kmask, lane);
+        while (__any_sync(kFull, pend != 0)) {
+          uint64_t cnd = 0ull;
+          if (pend) {
+            const int i = __ffs(pend) - 1;
+            pend &= pend - 1;
+            const float x = i == 0 ? e[0] : i == 1 ? e[1] : i == 2 ? e[2] : e[3];
+            cnd = make_cand(x, i0 + i);
+          }
+          warp_list_offer(entry, thr, cnd, k, kmask, lane);
+        }
       }
       // publish the warp's k-th entry; adopt a larger CTA-wide threshold
       if (lane == 0) atomicMax(&s_thr, (unsigned long long)thr);

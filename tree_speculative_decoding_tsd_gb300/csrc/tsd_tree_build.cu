@@ -37,6 +37,7 @@ struct TreeSmem {
   float f_sc[kMaxFront];
   int32_t f_depth[kMaxFront], f_par[kMaxFront], f_rank[kMaxFront];
   uint64_t f_w0[kMaxFront], f_w1[kMaxFront];
+  uint64_t f_key[kMaxFront];  // primary order key (smaller pops first)
   int32_t nf;
   // emitted rows
   float r_sc[kMaxD + 1];
@@ -49,6 +50,14 @@ struct TreeSmem {
 __device__ __forceinline__ void tuple_add(uint64_t& w0, uint64_t& w1, int level, uint64_t digit) {
   if (level < 12) w0 += digit << (59 - 5 * level);
   else w1 += digit << (59 - 5 * (level - 12));
+}
+
+// Primary key of a frontier entry: score descending (the bit pattern of a
+// non-negative float grows with it), then depth, then the first 27 tuple bits.
+// Entries with different keys are ordered by the key alone; equal keys (equal
+// score and depth, same leading ranks) are resolved by the full comparison.
+__device__ __forceinline__ uint64_t primary_key(float sc, int depth, uint64_t w0) {
+  return ((uint64_t)(~__float_as_uint(sc)) << 32) | ((uint64_t)depth << 27) | (w0 >> 37);
 }
 
 // true if frontier entry a precedes entry b in the total order
@@ -120,20 +129,39 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
     s.f_rank[0] = 0;
     s.f_w0[0] = 0ull;
     s.f_w1[0] = 0ull;
+    s.f_key[0] = primary_key(s.f_sc[0], 1, 0ull);
     s.nf = 1;
   }
   __syncwarp();
 
-  // ---- D pops ----
+  // ---- D pops: warp-wide minimum of the primary keys ----
   for (int row = 1; row <= D; ++row) {
     const int nf = s.nf;
+    uint64_t kmin = ~0ull;
     int best = -1;
-    for (int e = lane; e < nf; e += 32)
-      if (best < 0 || precedes(s, e, best)) best = e;
+    for (int e = lane; e < nf; e += 32) {
+      const uint64_t ke = s.f_key[e];
+      if (ke < kmin) { kmin = ke; best = e; }
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const int other = __shfl_xor_sync(kFull, best, off);
-      if (other >= 0 && (best < 0 || precedes(s, other, best))) best = other;
+      const uint64_t ok = __shfl_xor_sync(kFull, kmin, off);
+      const int oe = __shfl_xor_sync(kFull, best, off);
+      if (ok < kmin || (ok == kmin && oe >= 0 && (best < 0 || oe < best))) { kmin = ok; best = oe; }
+    }
+    // several entries with the same primary key: full comparison among them
+    int ties = 0;
+    for (int e = lane; e < nf; e += 32) ties += (s.f_key[e] == kmin) ? 1 : 0;
+    if (__popc(__ballot_sync(kFull, ties > 0)) > 1 || __any_sync(kFull, ties > 1)) {
+      int b2 = -1;
+      for (int e = lane; e < nf; e += 32)
+        if (s.f_key[e] == kmin && (b2 < 0 || precedes(s, e, b2))) b2 = e;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const int other = __shfl_xor_sync(kFull, b2, off);
+        if (other >= 0 && (b2 < 0 || precedes(s, other, b2))) b2 = other;
+      }
+      best = b2;
     }
     if (lane == 0 && best >= 0) {
       const float sc = s.f_sc[best];
@@ -154,12 +182,14 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       mask[o + row] = m;
       // the popped slot becomes the next sibling, or is removed
       if (rk + 1 < k) {
-        s.f_sc[best] = __fmul_rn(s.r_sc[par], s.tp[d - 1][rk + 1]);
-        s.f_rank[best] = rk + 1;
+        const float nsc = __fmul_rn(s.r_sc[par], s.tp[d - 1][rk + 1]);
         uint64_t nw0 = w0, nw1 = w1;
         tuple_add(nw0, nw1, d - 1, 1ull);
+        s.f_sc[best] = nsc;
+        s.f_rank[best] = rk + 1;
         s.f_w0[best] = nw0;
         s.f_w1[best] = nw1;
+        s.f_key[best] = primary_key(nsc, d, nw0);
       } else {
         const int last = s.nf - 1;
         s.f_sc[best] = s.f_sc[last];
@@ -168,17 +198,20 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
         s.f_rank[best] = s.f_rank[last];
         s.f_w0[best] = s.f_w0[last];
         s.f_w1[best] = s.f_w1[last];
+        s.f_key[best] = s.f_key[last];
         s.nf = last;
       }
       // first child (rank 0 at the next position)
       if (d < S) {
         const int e = s.nf;
-        s.f_sc[e] = __fmul_rn(sc, s.tp[d][0]);
+        const float csc = __fmul_rn(sc, s.tp[d][0]);
+        s.f_sc[e] = csc;
         s.f_depth[e] = d + 1;
         s.f_par[e] = row;
         s.f_rank[e] = 0;
         s.f_w0[e] = w0;
         s.f_w1[e] = w1;
+        s.f_key[e] = primary_key(csc, d + 1, w0);
         s.nf = e + 1;
       }
     }
