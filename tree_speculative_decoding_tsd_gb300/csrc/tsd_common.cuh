@@ -76,4 +76,24 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
   return v;
 }
 
+// Top-k of the 32*NC candidates held by the warp (NC per lane), returned as
+// a warp-distributed list (lane j holds the j-th largest, lanes >= k hold
+// whatever).  k rounds of a warp-wide maximum; the winner is removed from its
+// lane (candidates are distinct, so the winner is unique).  Missing
+// candidates are 0.  The lanes' arrays are consumed.
+template <int NC>
+__device__ __forceinline__ uint64_t warp_topk(uint64_t (&c)[NC], int k, int lane) {
+  uint64_t entry = 0ull;
+  for (int r = 0; r < k; ++r) {
+    uint64_t m = 0ull;
+#pragma unroll
+    for (int i = 0; i < NC; ++i) m = c[i] > m ? c[i] : m;
+    const uint64_t w = warp_max_u64(m);
+    if (lane == r) entry = w;
+#pragma unroll
+    for (int i = 0; i < NC; ++i) c[i] = (c[i] == w) ? 0ull : c[i];
+  }
+  return entry;
+}
+
 }  // namespace tsd

@@ -160,7 +160,24 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
       if (!have[u]) continue;
       hi = fmaxf(hi, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
     }
-    if (__any_sync(kFull, hi >= thr_v)) {
+    if (v0 == warp * 32) {
+      // first trip: the list is empty or nearly so and almost everything would
+      // be offered -- take the top-k of this trip plus the current list in k
+      // warp-wide rounds instead
+      uint64_t cb[17];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t i0 = (uint32_t)(a0 + 4 * (v0 + u * kScanThreads + lane));
+        cb[4 * u + 0] = have[u] ? make_cand(f[u].x, i0) : 0ull;
+        cb[4 * u + 1] = have[u] ? make_cand(f[u].y, i0 + 1) : 0ull;
+        cb[4 * u + 2] = have[u] ? make_cand(f[u].z, i0 + 2) : 0ull;
+        cb[4 * u + 3] = have[u] ? make_cand(f[u].w, i0 + 3) : 0ull;
+      }
+      cb[16] = lane < k ? entry : 0ull;
+      entry = warp_topk<17>(cb, k, lane);
+      thr = __shfl_sync(kFull, entry, k - 1);
+      if (lane == 0) atomicMax(&s_thr, (unsigned long long)thr);
+    } else if (__any_sync(kFull, hi >= thr_v)) {
       // only elements at or above the threshold value are offered: one warp
       // round per pending element of the busiest lane, per float4
 #pragma unroll
@@ -194,11 +211,10 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
   s_list[warp][lane] = entry;
   __syncthreads();
   if (warp == 0) {
-    thr = __shfl_sync(kFull, entry, k - 1);
-    for (int w = 1; w < kScanWarps; ++w) {
-      const uint64_t c = lane < k ? s_list[w][lane] : 0ull;
-      warp_list_offer(entry, thr, c, k, kmask, lane);
-    }
+    uint64_t cm[kScanWarps];
+#pragma unroll
+    for (int w = 0; w < kScanWarps; ++w) cm[w] = lane < k ? s_list[w][lane] : 0ull;
+    entry = warp_topk<kScanWarps>(cm, k, lane);
     if (lane < k) out[cta * k + lane] = entry;
   }
 }

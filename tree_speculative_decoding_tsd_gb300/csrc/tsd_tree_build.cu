@@ -28,21 +28,11 @@ namespace {
 constexpr int kMaxS = 16;
 constexpr int kMaxK = 32;
 constexpr int kMaxD = 64;
-constexpr int kMaxFront = kMaxD + 2;
 
 struct TreeSmem {
   float tp[kMaxS][kMaxK];     // top-k probabilities per position
   int32_t ti[kMaxS][kMaxK];   // top-k token ids per position
-  // frontier
-  float f_sc[kMaxFront];
-  int32_t f_depth[kMaxFront], f_par[kMaxFront], f_rank[kMaxFront];
-  uint64_t f_w0[kMaxFront], f_w1[kMaxFront];
-  uint64_t f_key[kMaxFront];  // primary order key (smaller pops first)
-  int32_t nf;
-  // emitted rows
-  float r_sc[kMaxD + 1];
-  int32_t r_par[kMaxD + 1];
-  uint64_t r_mask[kMaxD + 1], r_w0[kMaxD + 1], r_w1[kMaxD + 1];
+  uint8_t has_child[kMaxD + 1];
 };
 
 // Rank tuple of a path, 5 bits per level, most significant first, so that
@@ -60,12 +50,32 @@ __device__ __forceinline__ uint64_t primary_key(float sc, int depth, uint64_t w0
   return ((uint64_t)(~__float_as_uint(sc)) << 32) | ((uint64_t)depth << 27) | (w0 >> 37);
 }
 
-// true if frontier entry a precedes entry b in the total order
-__device__ __forceinline__ bool precedes(const TreeSmem& s, int a, int b) {
-  if (s.f_sc[a] != s.f_sc[b]) return s.f_sc[a] > s.f_sc[b];
-  if (s.f_depth[a] != s.f_depth[b]) return s.f_depth[a] < s.f_depth[b];
-  if (s.f_w0[a] != s.f_w0[b]) return s.f_w0[a] < s.f_w0[b];
-  return s.f_w1[a] < s.f_w1[b];
+// Full order between two frontier entries (score desc, depth asc, tuple asc).
+__device__ __forceinline__ bool precedes(float sa, int da, uint64_t a0, uint64_t a1, float sb,
+                                         int db, uint64_t b0, uint64_t b1) {
+  if (sa != sb) return sa > sb;
+  if (da != db) return da < db;
+  if (a0 != b0) return a0 < b0;
+  return a1 < b1;
+}
+
+// Per-lane register slots: frontier entry / row e lives in lane e % 32, slot e / 32.
+constexpr int kSlots = (kMaxD + 2 + 31) / 32;
+template <typename T>
+__device__ __forceinline__ T pick(const T (&v)[kSlots], int j) {
+  T r = v[0];
+#pragma unroll
+  for (int i = 1; i < kSlots; ++i) r = (j == i) ? v[i] : r;
+  return r;
+}
+template <typename T>
+__device__ __forceinline__ void put(T (&v)[kSlots], int j, T x, bool pred) {
+#pragma unroll
+  for (int i = 0; i < kSlots; ++i) v[i] = (pred && j == i) ? x : v[i];
+}
+template <typename T>
+__device__ __forceinline__ T bcast(const T (&v)[kSlots], int e) {
+  return __shfl_sync(kFull, pick(v, e >> 5), e & 31);
 }
 
 __global__ void __launch_bounds__(32 * kMaxS)
@@ -79,7 +89,6 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = D + 1;
   const long o = (long)b * R;
-  const unsigned kmask = (k >= 32) ? kFull : ((1u << k) - 1u);
 
   // ---- warp p merges the chunk lists of position p into its top-k ----
   // (at most kScanMaxCand candidates: every lane loads its share up front)
@@ -94,12 +103,7 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       const int i = lane + 32 * j;
       c[j] = i < ncand ? src[i] : 0ull;
     }
-    uint64_t entry = 0, thr = 0;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      if (32 * j >= ncand) break;
-      warp_list_offer(entry, thr, c[j], k, kmask, lane);
-    }
+    const uint64_t entry = warp_topk<kPer>(c, k, lane);
     if (lane < k) {
       s.tp[p][lane] = cand_val(entry);
       s.ti[p][lane] = (int32_t)cand_id(entry);
@@ -108,121 +112,139 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   __syncthreads();
   if (warp != 0) return;
 
-  // ---- root row and the first frontier entry (rank 0 at depth 1) ----
-  if (lane == 0) {
-    s.r_sc[0] = 1.0f;
-    s.r_par[0] = -1;
-    s.r_mask[0] = 0ull;
-    s.r_w0[0] = 0ull;
-    s.r_w1[0] = 0ull;
-    token[o] = root_tok[b];
-    parent[o] = -1;
-    depth[o] = 0;
-    score[o] = 1.0f;
-    mask[o] = 0ull;
-  }
-  __syncwarp();
-  if (lane == 0) {
-    s.f_sc[0] = __fmul_rn(1.0f, s.tp[0][0]);
-    s.f_depth[0] = 1;
-    s.f_par[0] = 0;
-    s.f_rank[0] = 0;
-    s.f_w0[0] = 0ull;
-    s.f_w1[0] = 0ull;
-    s.f_key[0] = primary_key(s.f_sc[0], 1, 0ull);
-    s.nf = 1;
-  }
-  __syncwarp();
-
-  // ---- D pops: warp-wide minimum of the primary keys ----
-  for (int row = 1; row <= D; ++row) {
-    const int nf = s.nf;
-    uint64_t kmin = ~0ull;
-    int best = -1;
-    for (int e = lane; e < nf; e += 32) {
-      const uint64_t ke = s.f_key[e];
-      if (ke < kmin) { kmin = ke; best = e; }
-    }
+  // ---- frontier and rows in registers, spread over the lanes ----
+  // A frontier entry also carries its parent's score and ancestor mask, so a
+  // pop needs no lookup of the parent row.
+  float f_sc[kSlots], f_psc[kSlots], r_sc[kSlots];
+  int32_t f_d[kSlots], f_par[kSlots], f_rk[kSlots], r_par[kSlots], r_tok[kSlots], r_dep[kSlots];
+  uint64_t f_w0[kSlots], f_w1[kSlots], f_key[kSlots], f_pm[kSlots], r_mask[kSlots];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const uint64_t ok = __shfl_xor_sync(kFull, kmin, off);
-      const int oe = __shfl_xor_sync(kFull, best, off);
-      if (ok < kmin || (ok == kmin && oe >= 0 && (best < 0 || oe < best))) { kmin = ok; best = oe; }
+  for (int j = 0; j < kSlots; ++j) {
+    f_sc[j] = 0.f; f_psc[j] = 0.f; f_d[j] = 0; f_par[j] = 0; f_rk[j] = 0;
+    f_w0[j] = 0ull; f_w1[j] = 0ull; f_key[j] = ~0ull; f_pm[j] = 0ull;
+    r_sc[j] = 0.f; r_par[j] = 0; r_tok[j] = 0; r_dep[j] = 0; r_mask[j] = 0ull;
+  }
+  // row 0 = root; frontier slot 0 = rank 0 at depth 1
+  if (lane == 0) {
+    r_sc[0] = 1.0f; r_par[0] = -1; r_tok[0] = root_tok[b]; r_dep[0] = 0; r_mask[0] = 0ull;
+    f_sc[0] = __fmul_rn(1.0f, s.tp[0][0]); f_psc[0] = 1.0f; f_d[0] = 1; f_par[0] = 0;
+    f_rk[0] = 0; f_pm[0] = 0ull;
+    f_key[0] = primary_key(f_sc[0], 1, 0ull);
+  }
+  int nf = 1;
+
+  for (int row = 1; row <= D; ++row) {
+    // this lane's smallest primary key, then the warp's: high word (score),
+    // then low word (depth, leading ranks) among the lanes that hold the high
+    uint64_t kmin = ~0ull;
+    int mine = -1;
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j) {
+      const int e = lane + 32 * j;
+      if (e < nf && f_key[j] < kmin) { kmin = f_key[j]; mine = e; }
     }
-    // several entries with the same primary key: full comparison among them
+    const unsigned hi = (unsigned)(kmin >> 32), lo = (unsigned)kmin;
+    const unsigned hmin = __reduce_min_sync(kFull, hi);
+    const unsigned lmin = __reduce_min_sync(kFull, hi == hmin ? lo : 0xffffffffu);
+    const bool holder = mine >= 0 && hi == hmin && lo == lmin;
+    const unsigned hb = __ballot_sync(kFull, holder);
     int ties = 0;
-    for (int e = lane; e < nf; e += 32) ties += (s.f_key[e] == kmin) ? 1 : 0;
-    if (__popc(__ballot_sync(kFull, ties > 0)) > 1 || __any_sync(kFull, ties > 1)) {
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j)
+      ties += (lane + 32 * j < nf && f_key[j] == ((uint64_t)hmin << 32 | lmin)) ? 1 : 0;
+    int best = __shfl_sync(kFull, mine, __ffs(hb) - 1);
+    if (__popc(hb) > 1 || __any_sync(kFull, ties > 1)) {
+      // equal primary keys (equal score, depth and leading ranks): full order
+      const uint64_t kk = (uint64_t)hmin << 32 | lmin;
       int b2 = -1;
-      for (int e = lane; e < nf; e += 32)
-        if (s.f_key[e] == kmin && (b2 < 0 || precedes(s, e, b2))) b2 = e;
+      float bs = 0.f; int bd = 0; uint64_t b0 = 0ull, b1 = 0ull;
+#pragma unroll
+      for (int j = 0; j < kSlots; ++j) {
+        const int e = lane + 32 * j;
+        if (e < nf && f_key[j] == kk &&
+            (b2 < 0 || precedes(f_sc[j], f_d[j], f_w0[j], f_w1[j], bs, bd, b0, b1))) {
+          b2 = e; bs = f_sc[j]; bd = f_d[j]; b0 = f_w0[j]; b1 = f_w1[j];
+        }
+      }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
-        const int other = __shfl_xor_sync(kFull, b2, off);
-        if (other >= 0 && (b2 < 0 || precedes(s, other, b2))) b2 = other;
+        const int oe = __shfl_xor_sync(kFull, b2, off);
+        const float os = __shfl_xor_sync(kFull, bs, off);
+        const int od = __shfl_xor_sync(kFull, bd, off);
+        const uint64_t o0 = __shfl_xor_sync(kFull, b0, off), o1 = __shfl_xor_sync(kFull, b1, off);
+        if (oe >= 0 && (b2 < 0 || precedes(os, od, o0, o1, bs, bd, b0, b1))) {
+          b2 = oe; bs = os; bd = od; b0 = o0; b1 = o1;
+        }
       }
       best = b2;
     }
-    if (lane == 0 && best >= 0) {
-      const float sc = s.f_sc[best];
-      const int d = s.f_depth[best];
-      const int par = s.f_par[best];
-      const int rk = s.f_rank[best];
-      const uint64_t w0 = s.f_w0[best], w1 = s.f_w1[best];
-      const uint64_t m = s.r_mask[par] | (1ull << (row - 1));
-      s.r_sc[row] = sc;
-      s.r_par[row] = par;
-      s.r_mask[row] = m;
-      s.r_w0[row] = w0;
-      s.r_w1[row] = w1;
-      token[o + row] = s.ti[d - 1][rk];
-      parent[o + row] = par;
-      depth[o + row] = d;
-      score[o + row] = sc;
-      mask[o + row] = m;
-      // the popped slot becomes the next sibling, or is removed
-      if (rk + 1 < k) {
-        const float nsc = __fmul_rn(s.r_sc[par], s.tp[d - 1][rk + 1]);
-        uint64_t nw0 = w0, nw1 = w1;
-        tuple_add(nw0, nw1, d - 1, 1ull);
-        s.f_sc[best] = nsc;
-        s.f_rank[best] = rk + 1;
-        s.f_w0[best] = nw0;
-        s.f_w1[best] = nw1;
-        s.f_key[best] = primary_key(nsc, d, nw0);
-      } else {
-        const int last = s.nf - 1;
-        s.f_sc[best] = s.f_sc[last];
-        s.f_depth[best] = s.f_depth[last];
-        s.f_par[best] = s.f_par[last];
-        s.f_rank[best] = s.f_rank[last];
-        s.f_w0[best] = s.f_w0[last];
-        s.f_w1[best] = s.f_w1[last];
-        s.f_key[best] = s.f_key[last];
-        s.nf = last;
-      }
-      // first child (rank 0 at the next position)
-      if (d < S) {
-        const int e = s.nf;
-        const float csc = __fmul_rn(sc, s.tp[d][0]);
-        s.f_sc[e] = csc;
-        s.f_depth[e] = d + 1;
-        s.f_par[e] = row;
-        s.f_rank[e] = 0;
-        s.f_w0[e] = w0;
-        s.f_w1[e] = w1;
-        s.f_key[e] = primary_key(csc, d + 1, w0);
-        s.nf = e + 1;
-      }
+    // the popped entry and the new row
+    const float sc = bcast(f_sc, best), psc = bcast(f_psc, best);
+    const int d = bcast(f_d, best), par = bcast(f_par, best), rk = bcast(f_rk, best);
+    const uint64_t w0 = bcast(f_w0, best), w1 = bcast(f_w1, best);
+    const uint64_t pm = bcast(f_pm, best);
+    const uint64_t m = pm | (1ull << (row - 1));
+    const int rl = row & 31, rj = row >> 5;
+    put(r_sc, rj, sc, lane == rl);
+    put(r_par, rj, par, lane == rl);
+    put(r_tok, rj, s.ti[d - 1][rk], lane == rl);
+    put(r_dep, rj, d, lane == rl);
+    put(r_mask, rj, m, lane == rl);
+    // the popped slot becomes the next sibling, or takes the last entry
+    const int bl = best & 31, bj = best >> 5;
+    const int last = nf - 1;
+    if (rk + 1 < k) {
+      const float nsc = __fmul_rn(psc, s.tp[d - 1][rk + 1]);
+      uint64_t nw0 = w0, nw1 = w1;
+      tuple_add(nw0, nw1, d - 1, 1ull);
+      const bool me = lane == bl;
+      put(f_sc, bj, nsc, me); put(f_rk, bj, rk + 1, me);
+      put(f_w0, bj, nw0, me); put(f_w1, bj, nw1, me);
+      put(f_key, bj, primary_key(nsc, d, nw0), me);
+    } else {
+      const float lsc = bcast(f_sc, last), lps = bcast(f_psc, last);
+      const int ld = bcast(f_d, last), lp = bcast(f_par, last), lr = bcast(f_rk, last);
+      const uint64_t l0 = bcast(f_w0, last), l1 = bcast(f_w1, last), lk = bcast(f_key, last);
+      const uint64_t lm = bcast(f_pm, last);
+      const bool me = lane == bl;
+      put(f_sc, bj, lsc, me); put(f_psc, bj, lps, me); put(f_d, bj, ld, me);
+      put(f_par, bj, lp, me); put(f_rk, bj, lr, me); put(f_w0, bj, l0, me);
+      put(f_w1, bj, l1, me); put(f_key, bj, lk, me); put(f_pm, bj, lm, me);
+      nf = last;
     }
-    __syncwarp();
+    // first child (rank 0 at the next position)
+    if (d < S) {
+      const float csc = __fmul_rn(sc, s.tp[d][0]);
+      const bool me = lane == (nf & 31);
+      const int cj = nf >> 5;
+      put(f_sc, cj, csc, me); put(f_psc, cj, sc, me); put(f_d, cj, d + 1, me);
+      put(f_par, cj, row, me); put(f_rk, cj, 0, me); put(f_w0, cj, w0, me);
+      put(f_w1, cj, w1, me); put(f_pm, cj, m, me);
+      put(f_key, cj, primary_key(csc, d + 1, w0), me);
+      ++nf;
+    }
   }
 
-  // ---- leaves ----
-  for (int r = lane; r < R; r += 32) {
-    bool has_child = false;
-    for (int c = 1; c < R; ++c) has_child |= (s.r_par[c] == r);
-    is_leaf[o + r] = has_child ? 0 : 1;
+  // ---- leaves and outputs (each lane writes its own rows) ----
+  for (int r = lane; r <= D; r += 32) s.has_child[r] = 0;
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < kSlots; ++j) {
+    const int r = lane + 32 * j;
+    if (r >= 1 && r <= D) s.has_child[r_par[j]] = 1;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < kSlots; ++j) {
+    const int r = lane + 32 * j;
+    if (r <= D) {
+      token[o + r] = r_tok[j];
+      parent[o + r] = r_par[j];
+      depth[o + r] = r_dep[j];
+      score[o + r] = r_sc[j];
+      mask[o + r] = r_mask[j];
+      is_leaf[o + r] = s.has_child[r] ? 0 : 1;
+    }
   }
 }
 
