@@ -28,12 +28,14 @@ scaling, no collective on the data path); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
 import subprocess
 import sys
 import tempfile
+import threading
 import time
 
 import numpy as np
@@ -140,11 +142,69 @@ def make_inputs(w, dev, rank):
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """SM clock and clock-event reasons sampled during the timed region.
 
-    def __init__(self, index):
+    Reads NVML through ctypes from a background thread every 0.2 ms (the timed
+    regions of the small workloads last a few milliseconds, shorter than one
+    nvidia-smi sampling period).  Falls back to `nvidia-smi -lms 100` when NVML
+    cannot be loaded.  Only reads: no clock or other GPU setting is changed."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, dev):
+        self.samples = []
+        self.t0 = self.t1 = None
+        self.max_mhz = None
         self.proc = None
-        self.path = None
+        self.thread = None
+        self.stop_flag = threading.Event()
+        try:
+            self._open_nvml(dev)
+        except (OSError, AttributeError, RuntimeError):
+            self.nvml = None
+            self._start_smi(dev.index if dev.index is not None else 0)
+            return
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+        deadline = time.perf_counter() + 2.0
+        while not self.samples and time.perf_counter() < deadline:
+            time.sleep(0.001)
+
+    def _open_nvml(self, dev):
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        try:
+            uuid = str(torch.cuda.get_device_properties(dev).uuid)
+            for u in (uuid, "GPU-" + uuid):
+                if nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0:
+                    ok = True
+                    break
+        except (AttributeError, RuntimeError):
+            pass
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(dev.index or 0, ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        self.nvml, self.h = nv, h
+        self.get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = int(mx.value)
+
+    def _poll(self):
+        mhz = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            t = time.perf_counter()
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0 and \
+                    self.get_reasons(self.h, ctypes.byref(rs)) == 0:
+                self.samples.append((t, int(mhz.value), int(rs.value)))
+            time.sleep(0.0002)
+
+    def _start_smi(self, index):
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
@@ -158,7 +218,25 @@ class Clocks:
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    def begin(self):
+        self.t0 = time.perf_counter()
+
+    def end(self):
+        self.t1 = time.perf_counter()
+
     def stop(self):
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=2)
+            win = [s for s in self.samples if self.t0 <= s[0] <= self.t1]
+            if not win:
+                return None
+            reasons = sorted({n for _, _, r in win for b, n in self.REASONS.items() if r & b})
+            return {"sm_mhz": statistics.median(s[1] for s in win), "sm_max_mhz": self.max_mhz,
+                    "samples": len(win), "source": "nvml, 0.2 ms period", "reasons": reasons}
+        return self._stop_smi()
+
+    def _stop_smi(self):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -178,7 +256,7 @@ class Clocks:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][1]),
-                "samples": len(rows), "reasons": reasons}
+                "samples": len(rows), "source": "nvidia-smi, 100 ms period", "reasons": reasons}
 
 
 def load_peaks():
@@ -210,8 +288,8 @@ def source_digest(files):
 
 CALL_SOURCES = {
     "build": ["tsd_tree_build.cu", "tsd_scan.cuh", "tsd_common.cuh"],
-    "verify": ["tsd_verify.cu", "tsd_verify_tc.cu", "tsd_verify_mma.cu", "tsd_verify.cuh",
-               "tsd_common.cuh"],
+    "verify": ["tsd_verify.cu", "tsd_verify_tc.cu", "tsd_verify_mla.cu", "tsd_verify_mma.cu",
+               "tsd_verify.cuh", "tsd_tcgen05.cuh", "tsd_common.cuh"],
     "accept": ["tsd_accept.cu", "tsd_scan.cuh", "tsd_common.cuh"],
     "commit": ["tsd_commit.cu", "tsd_common.cuh"],
 }
@@ -270,10 +348,11 @@ def run_ours(args, dist):
     # ---- timed region A: the whole step ----
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    clocks = Clocks(dev.index if dev.index is not None else 0)
+    clocks = Clocks(dev)
     dist.barrier()
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter()
+    clocks.begin()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
             prep()
@@ -284,6 +363,7 @@ def run_ours(args, dist):
                 one_step()
             ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
+    clocks.end()
     dist.barrier()
     t_wall = time.perf_counter() - t_wall
     clk = clocks.stop()

@@ -112,6 +112,7 @@ def test_tree_build_full_size(name):
     (4, 4, 2053, 8, 40, 256),       # heavy ties in the marginals
     (2, 3, 32, 32, 40, 16),         # V == k: every token kept, ties
     (3, 2, 200000, 4, 9, None),     # long rows over many chunks
+    (2, 3, 50000, 8, 20, 1),        # every probability rounds to 0: all elements tie
 ])
 def test_tree_build_edge_cases(B, S, V, k, D, quant):
     g = torch.Generator().manual_seed(B * 1000 + S * 100 + k)
@@ -490,4 +491,58 @@ def test_verify_paths_empty_and_tiny_prefixes(force_path):
     d = inputs("qwen", B=6, P=300, P_min=0, V=500)
     q, kc, vc, _, kt, vt = attn_inputs(w)
     plen = torch.tensor([0, 1, 127, 128, 129, 300], dtype=torch.int32)
+    check_attention(w, q, kc, vc, plen, kt, vt, d["tree"]["mask"])
+
+
+# ------------------------------------------------------ latent (MLA) heads --
+
+@pytest.mark.parametrize("force_path", ["tc", "generic"], indirect=True)
+def test_verify_latent_paths_splits_and_tails(force_path):
+    """Latent heads (dk 576, V = K[:, :512], 128 query heads): prefixes of
+    several 128-key tiles with ragged tails, split across CTAs and merged."""
+    d = inputs("mla", B=3, P=1300, P_min=200, V=2000)
+    w = d["w"]
+    check_attention(w, *attn_inputs(w), d["tree"]["mask"])
+
+
+@pytest.mark.parametrize("force_path", ["tc", "generic"], indirect=True)
+def test_verify_latent_empty_and_tiny_prefixes(force_path):
+    w = W.WORKLOADS["mla"].scaled(B=6, P=300, P_min=0, V=500)
+    d = inputs("mla", B=6, P=300, P_min=0, V=500)
+    q, kc, vc, _, kt, vt = attn_inputs(w)
+    plen = torch.tensor([0, 1, 127, 128, 129, 300], dtype=torch.int32)
+    check_attention(w, q, kc, vc, plen, kt, vt, d["tree"]["mask"])
+
+
+@pytest.mark.parametrize("force_path", ["tc", "generic"], indirect=True)
+def test_verify_latent_rescale_on_late_large_scores(force_path):
+    d = inputs("mla", B=2, P=900, P_min=900, V=2000)
+    w, tree = d["w"], d["tree"]
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    for b in range(w.B):
+        qd = q[b].float().mean(dim=(0, 1))
+        qd = qd / qd.norm()
+        for j, pos in enumerate(range(600, 900, 41)):
+            kc[b, 0, pos] = (qd * (6.0 + j)).to(kc.dtype)
+    check_attention(w, q, kc, vc, plen, kt, vt, tree["mask"])
+
+
+@pytest.mark.parametrize("name,force", [("qwen", "tc"), ("qwen", "mma"), ("qwen", "generic"),
+                                        ("mla", "tc"), ("mla", "generic")])
+def test_verify_ignores_nonfinite_cache_rows_past_prefix(name, force, monkeypatch):
+    """Cache rows at and past prefix_len hold NaN/Inf: tiles that straddle the
+    end of the prefix must not let them reach the output (0 x NaN)."""
+    monkeypatch.setenv("TSD_VERIFY_PATH", force)
+    over = dict(B=3, P=700, P_min=100, V=1000)
+    d = inputs(name, **over)
+    w = d["w"]
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    kc = kc.clone()
+    vc = None if vc is None else vc.clone()
+    for b in range(w.B):
+        p = int(plen[b])
+        kc[b, :, p:] = float("nan")
+        kc[b, :, p + 1::2] = float("inf")
+        if vc is not None:
+            vc[b, :, p:] = float("nan")
     check_attention(w, q, kc, vc, plen, kt, vt, d["tree"]["mask"])

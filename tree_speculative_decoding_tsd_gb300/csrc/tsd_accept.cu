@@ -131,7 +131,7 @@ using namespace tsd;
 extern "C" size_t tsd_accept_walk_workspace_size(int B, int D, int V) {
   if (B < 1 || D < 0 || V < 1) return 0;
   const long rows = (long)B * (D + 1);
-  const ScanGeom g = scan_geometry(rows, V, 1);
+  const ScanGeom g = scan_geometry(rows, V, 1, true);
   return (size_t)rows * g.nchunk * sizeof(uint64_t);
 }
 
@@ -154,7 +154,7 @@ extern "C" tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, 
   const cudaStream_t st = (cudaStream_t)stream;
   const int R = D + 1;
   const long rows = (long)B * R;
-  const ScanGeom g = scan_geometry(rows, V, 1);
+  const ScanGeom g = scan_geometry(rows, V, 1, true);
   uint64_t* part = (uint64_t*)ws;
   vocab_scan_kernel<true><<<(unsigned)(rows * g.nchunk), kScanThreads, 0, st>>>(
       logits, V, 1, g.nchunk, g.chunk_len, part);
@@ -225,7 +225,7 @@ extern "C" tsd_status tsd_accept_walk_static(const float* logits, int B, int D, 
   const cudaStream_t st = (cudaStream_t)stream;
   const int R = D + 1;
   const long rows = (long)B * R;
-  const ScanGeom g = scan_geometry(rows, V, 1);
+  const ScanGeom g = scan_geometry(rows, V, 1, true);
   vocab_scan_kernel<true><<<(unsigned)(rows * g.nchunk), kScanThreads, 0, st>>>(
       logits, V, 1, g.nchunk, g.chunk_len, part);
   accept_walk_kernel<<<B, 32 * kWalkWarps, 0, st>>>(part, R, S, g.nchunk, token, parent, mask, is_leaf, tgt,

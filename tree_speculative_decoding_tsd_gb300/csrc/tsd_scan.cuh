@@ -1,18 +1,20 @@
 // Vocabulary scan: per-chunk top-k (or argmax) of fp32 rows.
 //
 // Each row of length V is cut into `nchunk` chunks of `chunk_len` elements;
-// one 256-thread CTA scans one chunk with 16-byte streaming loads and writes
-// the chunk's k best candidates (64-bit keys, see make_cand) to
+// one 256-thread CTA scans one chunk with 16-byte loads and writes the
+// chunk's k best candidates (64-bit keys, see make_cand) to
 // out[row][chunk][0..k).  A second, per-request kernel merges the chunk lists:
 // the row's top-k is the top-k of the union of its chunks' top-k lists, which
 // is exact because candidates are distinct.
 //
-// Top-k mode keeps one sorted list per warp, one entry per lane.  An element
-// is offered to the list only when it beats the list threshold, which is the
-// larger of the warp's own k-th entry and a CTA-wide threshold published in
-// shared memory: k entries at least that large already exist, and keys are
-// distinct, so nothing at or below it can be in the chunk's top-k.  With
-// random rows almost every element is rejected by one compare.
+// Top-k mode reads the chunk once from HBM, keeping only a running maximum
+// per thread.  The k-th largest of the 256 thread maxima, T, is a cut-off:
+// k distinct elements are >= T, so every element of the chunk's top-k is
+// >= T, and only threads whose maximum reaches T hold any such element
+// (about k of the 256).  The warp re-reads just those threads' elements (from
+// L2, where the first pass left them) and offers the ones >= T to a sorted
+// warp list; the CTA then merges its eight warp lists.  NaN entries are never
+// selected.
 // Argmax mode (k = 1) keeps one running maximum per thread.
 #pragma once
 
@@ -22,8 +24,11 @@ namespace tsd {
 
 constexpr int kScanThreads = 256;
 constexpr int kScanWarps = kScanThreads / 32;
-// Partitioning assumes the GB300's 152 SMs with 8 resident scan CTAs each.
-constexpr int kScanTargetCtas = 152 * 8;
+// Partitioning assumes the GB300's 152 SMs with this many resident CTAs of
+// each mode (the launch bounds below enforce the register budget for it).
+constexpr int kScanSms = 152;
+constexpr int kScanArgmaxPerSm = 8;
+constexpr int kScanTopkPerSm = 4;
 constexpr int kScanMinChunk = 2048;
 // A row's chunk lists hold at most this many candidates, so the merge in the
 // consumer kernel reads a short, fixed-size list per row.
@@ -34,13 +39,24 @@ struct ScanGeom {
   int chunk_len;  // multiple of 256 elements
 };
 
-inline ScanGeom scan_geometry(long rows, int V, int k) {
-  long per_row = (kScanTargetCtas + rows - 1) / rows;
-  long max_chunks = (V + kScanMinChunk - 1) / kScanMinChunk;
-  if (per_row > max_chunks) per_row = max_chunks;
-  if (per_row > kScanMaxCand / k) per_row = kScanMaxCand / k;
-  if (per_row < 1) per_row = 1;
-  long len = (V + per_row - 1) / per_row;
+// Chunks per row: the count that minimises (waves of CTAs) x (chunk length +
+// fixed per-chunk cost), so that the last wave is not a small tail.  Host
+// code, no device query: workspace sizes follow from it and must not depend
+// on the GPU.
+inline ScanGeom scan_geometry(long rows, int V, int k, bool argmax) {
+  const long slots = (long)kScanSms * (argmax ? kScanArgmaxPerSm : kScanTopkPerSm);
+  const double overhead = argmax ? 512.0 : 4096.0;  // in element-times
+  long pmax = (V + kScanMinChunk - 1) / kScanMinChunk;
+  if (pmax > kScanMaxCand / k) pmax = kScanMaxCand / k;
+  if (pmax < 1) pmax = 1;
+  long best_p = 1;
+  double best_t = 1e300;
+  for (long p = 1; p <= pmax; ++p) {
+    const long waves = (rows * p + slots - 1) / slots;
+    const double t = (double)waves * ((double)V / (double)p + overhead);
+    if (t < best_t * 0.999) { best_t = t; best_p = p; }
+  }
+  long len = (V + best_p - 1) / best_p;
   len = (len + 255) / 256 * 256;
   ScanGeom g;
   g.chunk_len = (int)len;
@@ -51,11 +67,12 @@ inline ScanGeom scan_geometry(long rows, int V, int k) {
 __device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
 
 template <bool kArgmax>
-__global__ void __launch_bounds__(kScanThreads)
+__global__ void __launch_bounds__(kScanThreads, kArgmax ? kScanArgmaxPerSm : kScanTopkPerSm)
 vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chunk_len,
                   uint64_t* __restrict__ out) {
   __shared__ uint64_t s_list[kScanWarps][32];
-  __shared__ unsigned long long s_thr;
+  __shared__ float s_max[kScanThreads];
+  __shared__ float s_cut;
 
   const long cta = blockIdx.x;
   const long row = cta / nchunk;
@@ -122,89 +139,102 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
     return;
   }
 
-  // ---- top-k mode: warp lists -------------------------------------------
-  if (tid == 0) s_thr = 0ull;
-  __syncthreads();
+  // ---- top-k mode -------------------------------------------------------
+  // pass 1: stream the vector part once, one running maximum per thread
+  float m = -INFINITY;
+  {
+    int v = tid;
+    for (; v + 3 * kScanThreads < nvec; v += 4 * kScanThreads) {
+      float4 f[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) f[u] = __ldg(xv + v + u * kScanThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        m = fmaxf(m, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
+    }
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      if (v + u * kScanThreads < nvec) {
+        const float4 f = __ldg(xv + v + u * kScanThreads);
+        m = fmaxf(m, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+      }
+    }
+  }
+  s_max[tid] = m;
+
+  // the (at most 3 + 3) scalar edge elements are offered to the warp list directly
   const unsigned kmask = (k >= 32) ? kFull : ((1u << k) - 1u);
   uint64_t entry = 0, thr = 0;
-
-  // scalar edges: the whole warp offers one element per lane at a time
   for (int base = c0 + warp * 32; base < a0; base += kScanThreads) {
     const int i = base + lane;
-    const uint64_t c = i < a0 ? make_cand(xr[i], i) : 0ull;
+    const float x = i < a0 ? xr[i] : 0.f;
+    const uint64_t c = (i < a0 && x == x) ? make_cand(x, i) : 0ull;
     warp_list_offer(entry, thr, c, k, kmask, lane);
   }
   for (int base = a1 + warp * 32; base < c1; base += kScanThreads) {
     const int i = base + lane;
-    const uint64_t c = i < c1 ? make_cand(xr[i], i) : 0ull;
+    const float x = i < c1 ? xr[i] : 0.f;
+    const uint64_t c = (i < c1 && x == x) ? make_cand(x, i) : 0ull;
     warp_list_offer(entry, thr, c, k, kmask, lane);
   }
+  __syncthreads();
 
-  // main loop: every lane of the CTA takes 4 float4 per trip (warp-aligned so
-  // that the whole warp runs the same number of trips)
-  const int nvec_w = (nvec + 31) & ~31;
-  for (int v0 = warp * 32; v0 < nvec_w; v0 += 4 * kScanThreads) {
-    float4 f[4];
-    bool have[4];
+  // cut-off T: the k-th largest of the 256 thread maxima (k <= 32 < 256), by
+  // k rounds of a warp maximum over 32-bit order keys; each round removes one
+  // occurrence of the winner
+  if (warp == 0) {
+    uint32_t c[kScanThreads / 32];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int v = v0 + u * kScanThreads + lane;
-      have[u] = v < nvec;
-      f[u] = have[u] ? ld_stream(xv + v) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    // quick reject: nothing below the threshold's value can enter the list
-    const float thr_v = thr == 0ull ? -INFINITY : cand_val(thr);
-    float hi = -INFINITY;
+    for (int j = 0; j < kScanThreads / 32; ++j) c[j] = f32_order_key(s_max[j * 32 + lane]);
+    uint32_t w = 0;
+    for (int r = 0; r < k; ++r) {
+      uint32_t lm = c[0];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (!have[u]) continue;
-      hi = fmaxf(hi, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
-    }
-    if (v0 == warp * 32) {
-      // first trip: the list is empty or nearly so and almost everything would
-      // be offered -- take the top-k of this trip plus the current list in k
-      // warp-wide rounds instead
-      uint64_t cb[17];
+      for (int j = 1; j < kScanThreads / 32; ++j) lm = max(lm, c[j]);
+      w = __reduce_max_sync(kFull, lm);
+      const unsigned who = __ballot_sync(kFull, lm == w);
+      if (lane == __ffs(who) - 1) {
+        bool done = false;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t i0 = (uint32_t)(a0 + 4 * (v0 + u * kScanThreads + lane));
-        cb[4 * u + 0] = have[u] ? make_cand(f[u].x, i0) : 0ull;
-        cb[4 * u + 1] = have[u] ? make_cand(f[u].y, i0 + 1) : 0ull;
-        cb[4 * u + 2] = have[u] ? make_cand(f[u].z, i0 + 2) : 0ull;
-        cb[4 * u + 3] = have[u] ? make_cand(f[u].w, i0 + 3) : 0ull;
-      }
-      cb[16] = lane < k ? entry : 0ull;
-      entry = warp_topk<17>(cb, k, lane);
-      thr = __shfl_sync(kFull, entry, k - 1);
-      if (lane == 0) atomicMax(&s_thr, (unsigned long long)thr);
-    } else if (__any_sync(kFull, hi >= thr_v)) {
-      // only elements at or above the threshold value are offered: one warp
-      // round per pending element of the busiest lane, per float4
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
-        unsigned pend = 0;
-        if (have[u]) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) pend |= (e[i] >= thr_v) ? (1u << i) : 0u;
-        }
-        const uint32_t i0 = (uint32_t)(a0 + 4 * (v0 + u * kScanThreads + lane));
-        while (__any_sync(kFull, pend != 0)) {
-          uint64_t cnd = 0ull;
-          if (pend) {
-            const int i = __ffs(pend) - 1;
-            pend &= pend - 1;
-            const float x = i == 0 ? e[0] : i == 1 ? e[1] : i == 2 ? e[2] : e[3];
-            cnd = make_cand(x, i0 + i);
-          }
-          warp_list_offer(entry, thr, cnd, k, kmask, lane);
+        for (int j = 0; j < kScanThreads / 32; ++j) {
+          const bool hit = !done && c[j] == w;
+          c[j] = hit ? 0u : c[j];
+          done = done || hit;
         }
       }
-      // publish the warp's k-th entry; adopt a larger CTA-wide threshold
-      if (lane == 0) atomicMax(&s_thr, (unsigned long long)thr);
     }
-    const uint64_t shared_thr = *(volatile unsigned long long*)&s_thr;
-    thr = shared_thr > thr ? shared_thr : thr;
+    if (lane == 0) s_cut = order_key_f32(w);
+  }
+  __syncthreads();
+
+  // pass 2: the warp re-reads, one thread at a time, the elements of its
+  // threads whose maximum reaches T: lane j takes that thread's j-th float4
+  const float cut = s_cut;
+  unsigned act = __ballot_sync(kFull, m >= cut);
+  while (act) {
+    const int t = warp * 32 + __ffs(act) - 1;
+    act &= act - 1;
+    const int cnt = t < nvec ? (nvec - t + kScanThreads - 1) / kScanThreads : 0;
+    for (int j0 = 0; j0 < cnt; j0 += 32) {
+      const int j = j0 + lane;
+      const bool have = j < cnt;
+      const float4 f = have ? __ldg(xv + t + j * kScanThreads) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float e[4] = {f.x, f.y, f.z, f.w};
+      unsigned pend = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pend |= (have && e[i] >= cut) ? (1u << i) : 0u;
+      const uint32_t i0 = (uint32_t)(a0 + 4 * (t + j * kScanThreads));
+      while (__any_sync(kFull, pend != 0)) {
+        uint64_t cnd = 0ull;
+        if (pend) {
+          const int i = __ffs(pend) - 1;
+          pend &= pend - 1;
+          const float x = i == 0 ? e[0] : i == 1 ? e[1] : i == 2 ? e[2] : e[3];
+          cnd = make_cand(x, i0 + i);
+        }
+        warp_list_offer(entry, thr, cnd, k, kmask, lane);
+      }
+    }
   }
 
   // merge the warps' lists in warp 0

@@ -255,7 +255,7 @@ using namespace tsd;
 
 extern "C" size_t tsd_tree_build_workspace_size(int B, int S, int V, int k) {
   if (B < 1 || S < 1 || V < 1 || k < 1) return 0;
-  const ScanGeom g = scan_geometry((long)B * S, V, k);
+  const ScanGeom g = scan_geometry((long)B * S, V, k, false);
   return (size_t)B * S * g.nchunk * k * sizeof(uint64_t);
 }
 
@@ -276,7 +276,7 @@ extern "C" tsd_status tsd_tree_build(const float* probs, int B, int S, int V, in
   if (ws_bytes < need || !ok_ptr(ws)) return TSD_ERR_INVALID_ARG;
 
   const cudaStream_t st = (cudaStream_t)stream;
-  const ScanGeom g = scan_geometry((long)B * S, V, k);
+  const ScanGeom g = scan_geometry((long)B * S, V, k, false);
   const long ctas = (long)B * S * g.nchunk;
   uint64_t* part = (uint64_t*)ws;
   vocab_scan_kernel<false><<<(unsigned)ctas, kScanThreads, 0, st>>>(probs, V, k, g.nchunk,

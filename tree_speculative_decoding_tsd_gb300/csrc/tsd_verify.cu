@@ -19,10 +19,12 @@
 // Paths:
 //   generic (this file): CUDA-core fp32 arithmetic, one warp per key, lanes
 //     split the head dim, warp-shuffle reductions for q.k; any dtype/dims.
-//     Used for fp32 inputs (never TF32), for fewer than 64 packed rows (not
-//     a dense contraction) and for the latent (dk 576 / dv 512) heads.
+//     Used for fp32 inputs (never TF32) and for fewer than 64 packed rows (not
+//     a dense contraction).
 //   tc (tsd_verify_tc.cu): bf16 GQA heads, head dim 128, >= 64 packed rows:
 //     tcgen05 MMAs with TMEM accumulators, TMA-fed K/V ring (the default).
+//     Latent heads (bf16, dk 576 / dv 512, V = K[:, :512]) with >= 64 packed
+//     rows take the tcgen05 kernel of tsd_verify_mla.cu.
 //   mma (tsd_verify_mma.cu): bf16 GQA heads (head dim 64 or 128) with >= 64
 //     packed rows on the legacy warp-level mma.sync tensor-core path.
 #include <math.h>
@@ -170,7 +172,9 @@ verify_generic_kernel(VerifyArgs a) {
 static int choose_path(const tsd_attn_desc& d, int M) {
   const bool gqa_bf16 = d.dtype == TSD_BF16 && !d.v_aliases_k && d.dk == d.dv;
   const bool mma_ok = gqa_bf16 && (d.dk == 64 || d.dk == 128);
-  const bool tc_ok = gqa_bf16 && d.dk == 128 && M >= kMmaMinRows && tc_path_available();
+  const bool mla_bf16 = d.dtype == TSD_BF16 && d.v_aliases_k && d.dk == 576 && d.dv == 512;
+  const bool tc_ok = (gqa_bf16 && d.dk == 128 || mla_bf16) && M >= kMmaMinRows &&
+                     tc_path_available();
   const char* force = getenv("TSD_VERIFY_PATH");
   if (force != nullptr) {
     if (strcmp(force, "generic") == 0) return kPathGeneric;
@@ -188,7 +192,18 @@ VerifyPlan plan_verify(const tsd_attn_desc& d) {
   const int M = d.R * (d.Hq / d.Hkv);
   p.path = choose_path(d, M);
   long ns;
-  if (p.path == kPathTc) {
+  if (p.path == kPathTc && d.v_aliases_k) {
+    // latent heads: 64 packed rows per CTA (the MMA N), as many row groups as
+    // needed; splits only when the batch leaves the GPU short of CTAs (a split
+    // writes fp32 partial outputs of 512 dims per packed row)
+    p.nrg = (int)ceil_div(M, 64);
+    p.rb = 64;
+    const long units = (long)d.B * d.Hkv * p.nrg;
+    ns = ceil_div(152L * 2, units);
+    long len = ceil_div(ceil_div(d.cap, ns), 128) * 128;
+    if (len < 512) len = 512;
+    p.split_len = (int)len;
+  } else if (p.path == kPathTc) {
     // packed rows on the MMA N dimension: at most 144 per CTA, multiple of 16
     p.nrg = (int)ceil_div(M, 144);
     p.rb = (int)ceil_div(ceil_div(M, p.nrg), 16) * 16;
@@ -309,7 +324,8 @@ extern "C" tsd_status tsd_tree_verify_attn(const tsd_attn_desc* d, const void* q
   a.err = err;
   const cudaStream_t st = (cudaStream_t)stream;
   bool launched;
-  if (p.path == kPathTc) launched = launch_tc_path(*d, a, p, st);
+  if (p.path == kPathTc && d->v_aliases_k) launched = launch_mla_tc_path(*d, a, p, st);
+  else if (p.path == kPathTc) launched = launch_tc_path(*d, a, p, st);
   else if (p.path == kPathMma) launched = launch_mma_path(*d, a, p, st);
   else launched = launch_generic_path(*d, a, p, st);
   if (!launched) return TSD_ERR_UNSUPPORTED;

@@ -50,6 +50,8 @@ bool launch_mma_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPl
                      cudaStream_t st);
 bool launch_tc_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPlan& p,
                     cudaStream_t st);
+bool launch_mla_tc_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPlan& p,
+                        cudaStream_t st);
 bool tc_path_available();
 
 namespace {

@@ -40,6 +40,7 @@
 
 #include "tsd_common.cuh"
 #include "tsd_host.h"
+#include "tsd_tcgen05.cuh"
 #include "tsd_verify.cuh"
 
 namespace tsd {
@@ -57,7 +58,6 @@ constexpr uint32_t kOffV = 2 * kTileBytes;      // V ring: 2 x 32 KB
 constexpr uint32_t kOffQ = 4 * kTileBytes;      // 128 KB
 constexpr float kOverflow = 8.0f;               // log2 headroom of the lazy max
 constexpr int kPrefetch = 3;                    // prefix tiles prefetched into L2 ahead
-constexpr long long kWaitCycles = 2000000000ll; // ~1 s at 2 GHz
 
 template <int N>
 struct TcLayout {
@@ -84,181 +84,6 @@ struct TcLayout {
 // barrier indices
 enum { BAR_K_FULL = 0, BAR_K_EMPTY = 2, BAR_V_FULL = 4, BAR_V_EMPTY = 6, BAR_S_FULL = 8,
        BAR_P_FULL = 10, BAR_PV_DONE = 11, BAR_FINAL = 12 };
-
-__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-// Bounded wait for the phase with the given parity; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  const long long t0 = clock64();
-  for (;;) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
-    if (clock64() - t0 > kWaitCycles) return false;
-  }
-}
-
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                       uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
-                                       uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(map),
-               "r"(x), "r"(y)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-// 2^x on the special-function unit (PTX ex2.approx.ftz.f32: about 2 ulp,
-// results below 2^-126 flush to zero -- irrelevant for softmax weights)
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
-__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
-  uint32_t r[4];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, const float (&v)[4]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr),
-               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-               "r"(__float_as_uint(v[3])));
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
-
-// Named barrier over one warpgroup (128 threads) returning the OR of pred.
-__device__ __forceinline__ bool wg_bar_or(int wg, bool pred) {
-  uint32_t out;
-  asm volatile(
-      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
-      " bar.red.or.pred po, %2, 128, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
-      : "=r"(out)
-      : "r"((uint32_t)pred), "r"(1 + wg)
-      : "memory");
-  return out != 0;
-}
-__device__ __forceinline__ void wg_bar(int wg) {
-  asm volatile("bar.sync %0, 128;\n" ::"r"(1 + wg) : "memory");
-}
-
-// Reduce-scatter over the 32 lanes of a warp for a group of G columns held in
-// v[0..G): afterwards lane l holds, in v[0], the reduction over all 32 lanes of
-// column (l % G).  G is 8, 16 or 32; MAX selects max, else sum.
-template <int G, bool MAX>
-__device__ __forceinline__ float warp_reduce_scatter(float* v, int lane) {
-#pragma unroll
-  for (int s = G / 2; s >= 1; s >>= 1) {
-    const bool upper = lane & s;
-#pragma unroll
-    for (int i = 0; i < s; ++i) {
-      const float send = upper ? v[i] : v[i + s];
-      const float keep = upper ? v[i + s] : v[i];
-      const float recv = __shfl_xor_sync(kFull, send, s);
-      v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
-    }
-  }
-  float r = v[0];
-#pragma unroll
-  for (int s = G; s < 32; s <<= 1) {
-    const float o = __shfl_xor_sync(kFull, r, s);
-    r = MAX ? fmaxf(r, o) : r + o;
-  }
-  return r;
-}
-
-// Column reduction over the 32 lanes for the NH columns in x[]: the results
-// land in red[col] (one writer per column).
-template <int NH, bool MAX>
-__device__ __forceinline__ void warp_columns(const float* x, float* red, int lane) {
-  constexpr int n32 = NH / 32;
-  constexpr int rem = NH - 32 * n32;          // 0, 8, 16 or 24
-#pragma unroll
-  for (int gi = 0; gi < n32; ++gi) {
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = x[32 * gi + i];
-    const float r = warp_reduce_scatter<32, MAX>(v, lane);
-    red[32 * gi + lane] = r;
-  }
-  if (rem >= 16) {
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = x[32 * n32 + i];
-    const float r = warp_reduce_scatter<16, MAX>(v, lane);
-    if (lane < 16) red[32 * n32 + lane] = r;
-  }
-  if (rem % 16 == 8) {
-    constexpr int base = NH - 8;
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = x[base + i];
-    const float r = warp_reduce_scatter<8, MAX>(v, lane);
-    if (lane < 8) red[base + lane] = r;
-  }
-}
 
 struct TcMaps {
   CUtensorMap k, v, kt, vt;
@@ -709,25 +534,6 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
 }
 
 // --------------------------------------------------------------- host side
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeTiledFn)p;
-  });
-  return fn;
-}
 
 // rows x 128 bf16 (row pitch 256 B), boxes of [128 rows][64 cols], 128B swizzle
 bool encode_2d(CUtensorMap* m, const void* base, long rows) {
