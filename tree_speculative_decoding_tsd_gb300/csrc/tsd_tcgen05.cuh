@@ -64,6 +64,19 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int
       : "memory");
 }
 
+__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                       int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(map),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(map),
                "r"(x), "r"(y)
@@ -87,6 +100,18 @@ __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+// Accumulating MMA (D += A.B) without a runtime predicate.  Issue cost
+// matters: a single thread issuing MMAs whose descriptors are rebuilt from
+// addresses each time manages about one per 70 cycles, less than the tensor
+// core's rate for N <= 128; descriptors are therefore built once and advanced
+// by adding (byte offset >> 4) to their start-address field, which stays in
+// its 14 bits for any shared-memory address.
+__device__ __forceinline__ void mma_f16_acc(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, 1, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc));
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(

@@ -193,9 +193,9 @@ VerifyPlan plan_verify(const tsd_attn_desc& d) {
   p.path = choose_path(d, M);
   long ns;
   if (p.path == kPathTc && d.v_aliases_k) {
-    // latent heads: 64 packed rows per CTA (the MMA N), as many row groups as
-    // needed; splits only when the batch leaves the GPU short of CTAs (a split
-    // writes fp32 partial outputs of 512 dims per packed row)
+    // Splits only when the batch leaves the GPU short of CTAs (a split writes
+    // fp32 partial outputs of 512 dims per packed row).
+    // latent heads: 64 packed rows per CTA (the MMA N)
     p.nrg = (int)ceil_div(M, 64);
     p.rb = 64;
     const long units = (long)d.B * d.Hkv * p.nrg;

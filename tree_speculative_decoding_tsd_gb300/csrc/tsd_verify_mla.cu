@@ -14,24 +14,32 @@
 //   O^T[d][n]   += V_tile^T . P^T   4 M-tiles of 128 dims, N = 64, K = 128 keys
 // Tensor memory: S^T double-buffered (2 x 64 columns) and O^T (4 x 64), 384
 // of 512 columns.  Shared memory: Q^T resident (9 boxes of [64 rows][64 dims],
-// 72 KB), a 4-slot ring of K pieces ([128 keys][64 dims], 16 KB each), a
-// 2-slot ring of V units ([128 keys][128 dims] as two boxes, 32 KB each) and
-// P^T (16 KB).  A 128-key tile of latent rows is 144 KB, too large to stay
-// resident beside Q, so the value dims are loaded a second time for O^T;
-// every row-group CTA of a request reads the same tiles, so these loads are
-// served by L2.
+// 72 KB), a 4-slot ring of 32 KB boxes and P^T (16 KB).  A box is two 64-dim
+// pieces of 128 keys ([2][128 keys][64 dims], 128-byte swizzle), loaded by
+// one 3-D TMA copy; a tile takes five K boxes (pieces 0-1, ..., 6-7, 8 and an
+// out-of-range piece that the copy fills with zeros) and four V boxes (pieces
+// 2u, 2u+1: exactly the 128 dims of O^T M-tile u).  A 128-key tile of latent
+// rows is 144 KB, too large to stay resident beside Q, so the value dims are
+// loaded a second time; every row-group CTA of a request reads the same
+// tiles, so those loads are served by L2.
 //
-// Roles (576 threads): warps 0-15 softmax/epilogue (warpgroup w/4 owns 16 of
+// Issue rates set the design: the tensor core needs 48 cycles for an
+// M128 x N64 x K16 MMA, a thread issuing TMA copies manages about one per
+// ~300-600 cycles, and every wait/commit around an MMA batch costs a few
+// hundred cycles.  So boxes are large (8 MMAs per wait and commit), the S^T
+// and O^T MMAs are issued by two threads, and two warps issue the copies.
+//
+// Roles (640 threads): warps 0-15 softmax/epilogue (warpgroup w/4 owns 16 of
 // the 64 columns, warp w%4 owns TMEM lanes 32(w%4)..+31: 32 keys of a tile or
-// 32 dims of an O^T M-tile); warp 16 allocates TMEM and issues the MMAs (one
-// thread), and zeroes the value rows of keys past the valid range of a
-// partial tile (whole warp) so that 0 x garbage never reaches O; warp 17
-// issues the TMA loads (two threads, one per ring).
-// Softmax: the lazy-maximum scheme of the GQA tcgen05 path (an optimistic pass
-// with the running maximum, an exact recomputation when a score exceeds it by
-// more than 2^8 or on the first tile).  Every mbarrier wait is bounded; a
-// timeout sets TSD_DEV_ERR_TIMEOUT, all roles stop, in-flight copies and MMAs
-// are waited for and the tensor memory is released.
+// 32 dims of an O^T M-tile); warp 16 allocates TMEM and issues the S^T MMAs;
+// warp 17 issues the O^T MMAs (one thread) and zeroes the value rows of keys
+// past the valid range of a partial tile (whole warp) so that 0 x garbage
+// never reaches O; warps 18-19 issue the TMA copies (one thread each, boxes
+// alternating).  Softmax: the lazy-maximum scheme of the GQA tcgen05 path (an
+// optimistic pass with the running maximum, an exact recomputation when a
+// score exceeds it by more than 2^8 or on the first tile).  Every mbarrier
+// wait is bounded; a timeout sets TSD_DEV_ERR_TIMEOUT, all roles stop,
+// in-flight copies and MMAs are waited for and the tensor memory is released.
 #include "tsd_common.cuh"
 #include "tsd_host.h"
 #include "tsd_tcgen05.cuh"
@@ -42,16 +50,17 @@ namespace {
 
 constexpr int kKeys = 128;                      // keys per tile (MMA M of S^T)
 constexpr int kDK = 576, kDV = 512;
-constexpr int kKP = kDK / 64;                   // K pieces per tile
-constexpr int kVU = kDV / 128;                  // V units (O^T M-tiles) per tile
+constexpr int kKP = kDK / 64;                   // 64-dim pieces per key row
+constexpr int kKB = (kKP + 1) / 2;              // K boxes per tile
+constexpr int kVU = kDV / 128;                  // V boxes (O^T M-tiles) per tile
 constexpr int kSoftWarps = 16;
-constexpr int kThreads = (kSoftWarps + 2) * 32;
-constexpr int kMmaWarp = 16, kTmaWarp = 17;
-constexpr uint32_t kBox = kKeys * 128;          // [128 rows][64 bf16] swizzled box: 16 KB
-constexpr int kKSlots = 4, kVSlots = 2;
-constexpr uint32_t kOffK = 0;
-constexpr uint32_t kOffV = kKSlots * kBox;
-constexpr uint32_t kOffQ = kOffV + kVSlots * 2 * kBox;
+constexpr int kSWarp = 16, kOWarp = 17, kTmaWarp0 = 18, kTmaWarps = 2;
+constexpr int kThreads = (kSoftWarps + 2 + kTmaWarps) * 32;
+constexpr uint32_t kPiece = kKeys * 128;        // [128 rows][64 bf16] swizzled: 16 KB
+constexpr uint32_t kBox = 2 * kPiece;           // one ring slot
+constexpr int kSlots = 4;
+constexpr uint32_t kOffRing = 0;
+constexpr uint32_t kOffQ = kOffRing + kSlots * kBox;
 constexpr float kOverflow = 8.0f;               // log2 headroom of the lazy max
 constexpr int kPrefetch = 2;                    // prefix tiles prefetched into L2 ahead
 
@@ -60,7 +69,7 @@ struct MlaLayout {
   static constexpr uint32_t q_box = (uint32_t)N * 128u;   // one [N][64] box of Q^T
   static constexpr uint32_t off_pt = kOffQ + kKP * q_box;
   static constexpr uint32_t pt_blocks = (N + 63) / 64;
-  static constexpr uint32_t off_misc = off_pt + pt_blocks * kBox;
+  static constexpr uint32_t off_misc = off_pt + pt_blocks * kPiece;
   static constexpr int NH = N / 4;
   static constexpr uint32_t off_m = off_misc;
   static constexpr uint32_t off_alpha = off_m + 4 * N;
@@ -69,17 +78,18 @@ struct MlaLayout {
   static constexpr uint32_t off_rmask = (off_red + 4 * kSoftWarps * NH + 7) / 8 * 8;
   static constexpr uint32_t off_ooff = off_rmask + 8 * N;
   static constexpr uint32_t off_bar = off_ooff + 8 * N;
-  static constexpr int nbar = 17;
+  static constexpr int nbar = 16;
   static constexpr uint32_t off_flags = off_bar + 8 * nbar;
-  static constexpr uint32_t total = off_flags + 16;
+  static constexpr uint32_t total = off_flags + 16;  // [0] tmem [1] abort [2] K seen [3] V seen
   static_assert(q_box % 1024 == 0, "Q boxes must keep 1 KB swizzle alignment");
   static_assert(off_pt % 1024 == 0, "P^T must keep 1 KB swizzle alignment");
   static_assert(total + 1024 <= 232448, "shared memory budget");
   static_assert(6 * N <= 512, "tensor memory budget");
 };
 
-enum { BAR_K_FULL = 0, BAR_K_EMPTY = 4, BAR_V_FULL = 8, BAR_V_EMPTY = 10, BAR_S_FULL = 12,
-       BAR_P_FULL = 14, BAR_PV_DONE = 15, BAR_FINAL = 16 };
+enum { BAR_FULL = 0, BAR_EMPTY = kSlots, BAR_S_FULL = 2 * kSlots, BAR_S_FREE = 2 * kSlots + 2,
+       BAR_P_FULL = 2 * kSlots + 4, BAR_PV_DONE = 2 * kSlots + 5, BAR_FIN_S = 2 * kSlots + 6,
+       BAR_FIN_O = 2 * kSlots + 7 };
 
 struct MlaMaps {
   CUtensorMap k, kt;
@@ -120,44 +130,72 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_p
   // keys of tile t that exist (the rest are masked and their values zeroed)
   auto nvalid_of = [&](int t) { return t >= n_pre ? a.R : min(kKeys, k1 - (k0 + t * kKeys)); };
 
+  // The ring carries one sequence of boxes, in the order the MMAs use them:
+  //   K_0 (5 boxes), K_1, V_0 (4 boxes), K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}.
+  // Box i goes to slot i % 4 as that slot's (i / 4)-th load, so the phase of
+  // every FULL / EMPTY wait follows from the position alone.
+  auto step_start = [&](int s) { return kKB * s + kVU * (s > 0 ? s - 1 : 0); };
+  auto pos_k = [&](int t, int j) { return step_start(t) + j; };
+  auto pos_v = [&](int t, int u) { return step_start(t + 1) + (t + 1 < ntiles ? kKB : 0) + u; };
+  const int nbox = (kKB + kVU) * ntiles;
+  // The K boxes are consumed by one thread and the V boxes by another, each in
+  // its own order.  A parity wait is only sound while the barrier is at most
+  // one phase behind its target, so before waiting for position p a consumer
+  // makes sure the box at p - 4 (same slot, previous load) has been seen to
+  // land: its own kind by program order, the other kind through the other
+  // consumer's count of boxes seen (flags[2] for K, flags[3] for V).
+  // Returns -1 for "none needed", else 2 * index + (1 if a V box).
+  auto prev_box = [&](int p) {
+    const int q = p - kSlots;
+    if (q < 0) return -1;
+    if (q < kKB) return 2 * q;                      // K_0 box q
+    const int s2 = 1 + (q - kKB) / (kKB + kVU), r = (q - kKB) % (kKB + kVU);
+    if (s2 < ntiles && r < kKB) return 2 * (s2 * kKB + r);
+    return 2 * ((s2 - 1) * kVU + r - (s2 < ntiles ? kKB : 0)) + 1;
+  };
+  // wait until the other consumer has seen box `idx` of its kind land (bounded)
+  auto seen_by_other = [&](int counter, int idx) {
+    const long long t0 = clock64();
+    while ((int)flags[counter] <= idx) {
+      if (flags[1] || clock64() - t0 > kWaitCycles) return false;
+    }
+    return true;
+  };
+
   auto ycoord = [&](int t) { return (b * a.Hkv + hk) * a.cap + k0 + t * kKeys; };
-  // K piece p (dims 64p..64p+63) of tile t
-  auto tma_piece = [&](uint32_t dst, int t, int x, uint32_t fb) {
-    if (t < n_pre) tma_2d(dst, &maps.k, x, ycoord(t), fb);
-    else tma_3d(dst, &maps.kt, x, hk, b * a.R, fb);
+  // box of pieces z, z+1 of tile t
+  auto load_box = [&](uint32_t dst, int t, int z, uint32_t fb) {
+    if (t < n_pre) tma_3d(dst, &maps.k, 0, ycoord(t), z, fb);
+    else tma_4d(dst, &maps.kt, 0, hk, b * a.R, z, fb);
   };
   auto prefetch = [&](int t) {
     if (t < n_pre) {
 #pragma unroll 1
-      for (int p = 0; p < kKP; ++p) tma_prefetch_2d(&maps.k, 64 * p, ycoord(t));
+      for (int j = 0; j < kKB; ++j) tma_prefetch_3d(&maps.k, 0, ycoord(t), 2 * j);
     }
   };
 
   // ---------------------------------------------------------------- set-up
-  if (tid == kTmaWarp * 32) {
-    for (int s = 0; s < kKSlots; ++s) {
-      mbar_init(bar(BAR_K_FULL + s), 1);
-      mbar_init(bar(BAR_K_EMPTY + s), 1);
+  if (tid == kTmaWarp0 * 32) {
+    for (int sl = 0; sl < kSlots; ++sl) {
+      mbar_init(bar(BAR_FULL + sl), 1);
+      mbar_init(bar(BAR_EMPTY + sl), 1);
     }
-    for (int s = 0; s < kVSlots; ++s) {
-      mbar_init(bar(BAR_V_FULL + s), 1);
-      mbar_init(bar(BAR_V_EMPTY + s), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(BAR_S_FULL + i), 1);
+      mbar_init(bar(BAR_S_FREE + i), kSoftWarps);
     }
-    mbar_init(bar(BAR_S_FULL), 1);
-    mbar_init(bar(BAR_S_FULL + 1), 1);
     mbar_init(bar(BAR_P_FULL), kSoftWarps);
     mbar_init(bar(BAR_PV_DONE), 1);
-    mbar_init(bar(BAR_FINAL), 1);
+    mbar_init(bar(BAR_FIN_S), 1);
+    mbar_init(bar(BAR_FIN_O), 1);
     flags[1] = 0;
+    flags[2] = 0;
+    flags[3] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    // the first ring fill needs no free slot: start it before the set-up sync
-    for (int p = 0; p < kKSlots; ++p) {
-      mbar_expect_tx(bar(BAR_K_FULL + p), kBox);
-      tma_piece(sbase + kOffK + p * kBox, 0, 64 * p, bar(BAR_K_FULL + p));
-    }
     for (int t = 0; t < 1 + kPrefetch; ++t) prefetch(t);
   }
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
         sbase + L::off_flags));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
@@ -195,94 +233,95 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_p
   fence_after();
   const uint32_t tmem = flags[0];
   const uint32_t tm_s[2] = {tmem, tmem + (uint32_t)N};
-  const uint32_t tm_o = tmem + 2u * N;            // M-tile j at tm_o + j * N
+  const uint32_t tm_o = tmem + 2u * N;            // M-tile u at tm_o + u * N
+  const uint32_t idesc_qk = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+                            ((uint32_t)(kKeys >> 4) << 24);
+  const uint32_t idesc_pv = idesc_qk | (1u << 15) | (1u << 16);
 
   // ------------------------------------------------------------------ TMA
-  // Two producer threads, one per ring, each in the order the MMAs consume
-  // its loads (K pieces of S_0, S_1, ...; V units of O_0, O_1, ...), so that
-  // neither ring waits on the other.
-  if (warp == kTmaWarp) {
+  if (warp >= kTmaWarp0) {
+    const int w = warp - kTmaWarp0;
     if (lane == 0) {
-      int kc = kKSlots;   // the set-up filled the ring with pieces 0..3 of tile 0
-      bool stop = false;
-      for (int t = 0; t < ntiles && !stop; ++t) {
-        if (t > 0) prefetch(t + kPrefetch);
-        for (int p = (t == 0 ? kKSlots : 0); p < kKP; ++p) {
-          const int s = kc % kKSlots;
-          if (flags[1] || !mbar_wait(bar(BAR_K_EMPTY + s), ((kc / kKSlots) - 1) & 1)) {
-            stop = true;
-            break;
+      bool ok = true;
+      int p = 0;
+      auto put = [&](int t, int z) {
+        if (ok && p % kTmaWarps == w) {
+          const int sl = p % kSlots;
+          if (p >= kSlots && (flags[1] || !mbar_wait(bar(BAR_EMPTY + sl), ((p / kSlots) - 1) & 1))) {
+            ok = false;
+          } else {
+            mbar_expect_tx(bar(BAR_FULL + sl), kBox);
+            load_box(sbase + kOffRing + sl * kBox, t, z, bar(BAR_FULL + sl));
           }
-          mbar_expect_tx(bar(BAR_K_FULL + s), kBox);
-          tma_piece(sbase + kOffK + s * kBox, t, 64 * p, bar(BAR_K_FULL + s));
-          ++kc;
         }
+        ++p;
+      };
+      for (int s = 0; ok && s <= ntiles; ++s) {
+        if (s < ntiles) {
+          if (w == 0 && s > 0) prefetch(s + kPrefetch);
+          for (int j = 0; j < kKB; ++j) put(s, 2 * j);
+        }
+        if (s > 0)
+          for (int u = 0; u < kVU; ++u) put(s - 1, 2 * u);
       }
-      if (stop) flags[1] = 1;
+      if (!ok) flags[1] = 1;
       // no copy may still be in flight when the CTA leaves
-      for (int s = 0; s < kKSlots; ++s) {
-        const int c = (kc - s + kKSlots - 1) / kKSlots;
-        if (c > 0) mbar_wait(bar(BAR_K_FULL + s), (c - 1) & 1);
-      }
-    } else if (lane == 1) {
-      int vc = 0;
-      bool stop = false;
-      for (int t = 0; t < ntiles && !stop; ++t) {
-        for (int u = 0; u < kVU; ++u) {
-          const int s = vc % kVSlots;
-          if (flags[1] ||
-              (vc >= kVSlots && !mbar_wait(bar(BAR_V_EMPTY + s), ((vc / kVSlots) - 1) & 1))) {
-            stop = true;
-            break;
-          }
-          const uint32_t dst = sbase + kOffV + s * 2 * kBox;
-          mbar_expect_tx(bar(BAR_V_FULL + s), 2 * kBox);
-          tma_piece(dst, t, 128 * u, bar(BAR_V_FULL + s));
-          tma_piece(dst + kBox, t, 128 * u + 64, bar(BAR_V_FULL + s));
-          ++vc;
+      if (w == 0)
+        for (int sl = 0; sl < kSlots && sl < nbox; ++sl) {
+          const int last = sl + ((nbox - 1 - sl) / kSlots) * kSlots;
+          mbar_wait(bar(BAR_FULL + sl), (last / kSlots) & 1);
         }
-      }
-      if (stop) flags[1] = 1;
-      for (int s = 0; s < kVSlots; ++s) {
-        const int c = (vc - s + kVSlots - 1) / kVSlots;
-        if (c > 0) mbar_wait(bar(BAR_V_FULL + s), (c - 1) & 1);
-      }
     }
   }
 
-  // ------------------------------------------------------------------ MMA
-  else if (warp == kMmaWarp) {
-    const uint32_t idesc_qk = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-                              ((uint32_t)(kKeys >> 4) << 24);
-    const uint32_t idesc_pv = idesc_qk | (1u << 15) | (1u << 16);
-    const uint32_t qa = sbase + kOffQ, pta = sbase + L::off_pt;
-    int kc = 0, vc = 0;
-    auto issue_qk = [&](int t) -> bool {
-      const int st = t & 1;
-      for (int p = 0; p < kKP; ++p) {
-        const int s = kc % kKSlots;
-        if (!__all_sync(kFull, mbar_wait(bar(BAR_K_FULL + s), (kc / kKSlots) & 1))) return false;
-        fence_after();
-        if (lane == 0) {
-          const uint32_t kb = sbase + kOffK + s * kBox;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc(kb + kk * 32, 16, 1024);
-            const uint64_t bd = smem_desc(qa + p * L::q_box + kk * 32, 16, 1024);
-            mma_f16(tm_s[st], ad, bd, idesc_qk, (p > 0 || kk > 0) ? 1u : 0u);
+  // -------------------------------------------------------------- S^T MMAs
+  else if (warp == kSWarp) {
+    if (lane == 0) {
+      const uint64_t kd0 = smem_desc(sbase + kOffRing, 16, 1024);
+      const uint64_t qd0 = smem_desc(sbase + kOffQ, 16, 1024);
+      bool ok = true;
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int st = t & 1;
+        // S^T buffer st was last read by the softmax of tile t - 2
+        if (t >= 2 && !mbar_wait(bar(BAR_S_FREE + st), ((t >> 1) - 1) & 1)) { ok = false; break; }
+        for (int j = 0; j < kKB; ++j) {
+          const int p = pos_k(t, j), sl = p % kSlots, pv = prev_box(p);
+          if ((pv >= 0 && (pv & 1) && !seen_by_other(3, pv >> 1)) || flags[1] ||
+              !mbar_wait(bar(BAR_FULL + sl), (p / kSlots) & 1)) {
+            ok = false;
+            break;
           }
-          mma_commit(bar(BAR_K_EMPTY + s));
+          __threadfence_block();
+          flags[2] = (uint32_t)(t * kKB + j + 1);
+          fence_after();
+          const uint64_t ad = kd0 + (uint64_t)(sl * (kBox >> 4));
+          const uint64_t bd = qd0 + (uint64_t)(2 * j * (L::q_box >> 4));
+          if (j == 0) mma_f16(tm_s[st], ad, bd, idesc_qk, 0u);
+          else mma_f16_acc(tm_s[st], ad, bd, idesc_qk);
+#pragma unroll
+          for (int kk = 1; kk < 4; ++kk) mma_f16_acc(tm_s[st], ad + 2 * kk, bd + 2 * kk, idesc_qk);
+          if (2 * j + 1 < kKP) {
+            const uint64_t ad1 = ad + (kPiece >> 4), bd1 = bd + (L::q_box >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_f16_acc(tm_s[st], ad1 + 2 * kk, bd1 + 2 * kk, idesc_qk);
+          }
+          mma_commit(bar(BAR_EMPTY + sl));
         }
-        __syncwarp();
-        ++kc;
+        if (ok) mma_commit(bar(BAR_S_FULL + st));
       }
-      if (lane == 0) mma_commit(bar(BAR_S_FULL + st));
-      __syncwarp();
-      return true;
-    };
-    bool ok = issue_qk(0);
+      if (!ok) flags[1] = 1;
+      // every MMA issued by this thread has completed once this commit lands
+      mma_commit(bar(BAR_FIN_S));
+      mbar_wait(bar(BAR_FIN_S), 0);
+    }
+  }
+
+  // -------------------------------------------------------------- O^T MMAs
+  else if (warp == kOWarp) {
+    const uint64_t vd0 = smem_desc(sbase + kOffRing, kPiece, 1024);
+    const uint64_t ptd0 = smem_desc(sbase + L::off_pt, kPiece, 1024);
+    bool ok = true;
     for (int t = 0; ok && t < ntiles; ++t) {
-      if (t + 1 < ntiles && !issue_qk(t + 1)) { ok = false; break; }
       if (!__all_sync(kFull, mbar_wait(bar(BAR_P_FULL), t & 1)) ||
           __any_sync(kFull, flags[1] != 0)) {
         ok = false;
@@ -290,20 +329,24 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_p
       }
       const int nvalid = nvalid_of(t);
       for (int u = 0; u < kVU; ++u) {
-        const int s = vc % kVSlots;
-        if (!__all_sync(kFull, mbar_wait(bar(BAR_V_FULL + s), (vc / kVSlots) & 1))) {
+        const int p = pos_v(t, u), sl = p % kSlots, pv = prev_box(p);
+        const bool prev_ok = pv < 0 || (pv & 1) || seen_by_other(2, pv >> 1);
+        if (!__all_sync(kFull, prev_ok && mbar_wait(bar(BAR_FULL + sl), (p / kSlots) & 1))) {
           ok = false;
           break;
         }
-        const uint32_t vb = kOffV + s * 2 * kBox;
+        if (lane == 0) {
+          __threadfence_block();
+          flags[3] = (uint32_t)(t * kVU + u + 1);
+        }
         if (nvalid < kKeys) {
           // value rows of keys past the range may hold anything: zero them
           for (int key = nvalid + lane; key < kKeys; key += 32) {
-            uint8_t* r0 = smem + vb + key * 128u;
+            uint8_t* r0 = smem + kOffRing + sl * kBox + key * 128u;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               *(uint4*)(r0 + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-              *(uint4*)(r0 + kBox + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+              *(uint4*)(r0 + kPiece + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
             }
           }
           asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -311,27 +354,24 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_p
         }
         fence_after();
         if (lane == 0) {
+          const uint64_t ad = vd0 + (uint64_t)(sl * (kBox >> 4));
+          if (t == 0) mma_f16(tm_o + u * N, ad, ptd0, idesc_pv, 0u);
+          else mma_f16_acc(tm_o + u * N, ad, ptd0, idesc_pv);
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint64_t ad = smem_desc(sbase + vb + kk * 2048, kBox, 1024);
-            const uint64_t bd = smem_desc(pta + kk * 2048, kBox, 1024);
-            mma_f16(tm_o + u * N, ad, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(BAR_V_EMPTY + s));
+          for (int kk = 1; kk < kKeys / 16; ++kk)
+            mma_f16_acc(tm_o + u * N, ad + 128 * kk, ptd0 + 128 * kk, idesc_pv);
+          mma_commit(bar(BAR_EMPTY + sl));
         }
         __syncwarp();
-        ++vc;
       }
       if (!ok) break;
       if (lane == 0) mma_commit(bar(BAR_PV_DONE));
       __syncwarp();
     }
     if (!ok && lane == 0) flags[1] = 1;
-    // every MMA issued so far has completed once this commit lands: wait for
-    // it before the TMEM is released
     if (lane == 0) {
-      mma_commit(bar(BAR_FINAL));
-      mbar_wait(bar(BAR_FINAL), 0);
+      mma_commit(bar(BAR_FIN_O));
+      mbar_wait(bar(BAR_FIN_O), 0);
     }
     __syncwarp();
   }
@@ -447,6 +487,10 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_p
           pp[2 * j + 1] = pack_bf16x2(v[2], v[3]);
         }
       }
+      // every read of S^T is done: its buffer may take tile t + 2
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_S_FREE + st));
       // P^T is single-buffered: the previous tile's O^T products must be done
       if (t > 0 && !__all_sync(kFull, mbar_wait(bar(BAR_PV_DONE), (t - 1) & 1))) failed = true;
       fence_after();
@@ -470,7 +514,7 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_p
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
         const int n0 = c0 + 4 * j;
-        const uint32_t off = L::off_pt + (n0 >> 6) * kBox + key * 128u +
+        const uint32_t off = L::off_pt + (n0 >> 6) * kPiece + key * 128u +
                              ((((n0 & 63) >> 3) ^ (key & 7)) << 4) + ((n0 & 4) << 1);
         *(uint2*)(smem + off) = make_uint2(pp[2 * j], pp[2 * j + 1]);
       }
@@ -544,31 +588,34 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_p
   __syncthreads();
   if (flags[1] && tid == 0) report_error(a.err, TSD_DEV_ERR_TIMEOUT, b);
   fence_after();
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem));
   }
 }
 
-// rows x 576 bf16 (row pitch 1152 B), boxes of [128 rows][64 dims], 128B swizzle
-bool encode_latent_2d(CUtensorMap* m, const void* base, long rows) {
-  const cuuint64_t dims[2] = {(cuuint64_t)kDK, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kDK * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)kKeys};
-  const cuuint32_t es[2] = {1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+// Latent rows [rows][576] bf16 viewed as (64 dims, rows, 9 pieces) with
+// strides (1152 B, 128 B): a box of (64, 128 rows, 2 pieces) lands as
+// [2][128][64] with 128-byte swizzle; pieces past the 9th read as zeros.
+bool encode_latent(CUtensorMap* m, const void* base, long rows) {
+  const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)kKP};
+  const cuuint64_t strides[2] = {(cuuint64_t)kDK * 2, 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kKeys, 2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [B*R][Hkv][576] bf16, boxes of [128 rows][1 head][64 dims]
-bool encode_latent_3d(CUtensorMap* m, const void* base, int Hkv, long rows) {
-  const cuuint64_t dims[3] = {(cuuint64_t)kDK, (cuuint64_t)Hkv, (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {(cuuint64_t)kDK * 2, (cuuint64_t)Hkv * kDK * 2};
-  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kKeys};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+// Tree rows [B*R][Hkv][576] bf16 as (64 dims, Hkv, B*R, 9 pieces), boxes of
+// (64, 1 head, 128 rows, 2 pieces); rows past B*R read as zeros.
+bool encode_latent_tree(CUtensorMap* m, const void* base, int Hkv, long rows) {
+  const cuuint64_t dims[4] = {64, (cuuint64_t)Hkv, (cuuint64_t)rows, (cuuint64_t)kKP};
+  const cuuint64_t strides[3] = {(cuuint64_t)kDK * 2, (cuuint64_t)Hkv * kDK * 2, 128};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kKeys, 2};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -590,8 +637,8 @@ bool launch_mla_tc_path(const tsd_attn_desc& d, const VerifyArgs& a, const Verif
   if (d.dk != kDK || d.dv != kDV || !d.v_aliases_k || d.dtype != TSD_BF16) return false;
   if (encode_fn() == nullptr || p.rb != 64) return false;
   MlaMaps maps;
-  if (!encode_latent_2d(&maps.k, a.kc, (long)d.B * d.Hkv * d.cap) ||
-      !encode_latent_3d(&maps.kt, a.kt, d.Hkv, (long)d.B * d.R))
+  if (!encode_latent(&maps.k, a.kc, (long)d.B * d.Hkv * d.cap) ||
+      !encode_latent_tree(&maps.kt, a.kt, d.Hkv, (long)d.B * d.R))
     return false;
   launch_mla<64>(maps, a, p, st);
   if (p.nsplit > 1) {

@@ -12,9 +12,9 @@
 // Roles (576 threads): warps 0-15 softmax/epilogue (warpgroup w/4 owns a
 // quarter of the columns, warp w%4 owns TMEM lanes 32(w%4)..+31, i.e. 32 keys
 // of a tile or 32 dims of O^T); warp 16 allocates TMEM and issues the MMAs
-// (one thread); warp 17 issues the TMA loads (one thread).  K and V tiles of 128 keys (32 KB
-// each) arrive by cp.async.bulk.tensor with 128-byte swizzle into two separate
-// two-stage rings: a K stage is refilled as soon as its S^T product is done, a V
+// (one thread); warp 17 issues the TMA loads (one thread per ring).  K and V
+// tiles of 128 keys (32 KB each) arrive by cp.async.bulk.tensor with 128-byte
+// swizzle into two separate two-stage rings: a K stage is refilled as soon as its S^T product is done, a V
 // stage as soon as its O^T product is done, so each load is issued about two
 // tiles ahead of its use.  mbarriers order TMA -> MMA -> softmax -> MMA.
 //
@@ -221,32 +221,35 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
   const uint32_t tm_o = tmem + 2u * N;
 
   // ------------------------------------------------------------------ TMA
+  // One thread per ring (a thread completes about one TMA box per ~570
+  // cycles, so the K and V streams are issued side by side): K_t after
+  // S^T_{t-2} freed its stage, V_t after O^T_{t-2} freed its stage.
   if (warp == kTmaWarp) {
     if (lane == 0) {
-      // Loads in the order their stages free up: K_t after S^T_{t-2}, then
-      // V_{t-1} after O^T_{t-3} (the MMA completes in issue order).
-      int nk = ntiles > 1 ? 2 : 1, nv = 1;
-      for (int t = 2; t <= ntiles && !flags[1]; ++t) {
-        if (t < ntiles) {
-          if (!mbar_wait(bar(BAR_K_EMPTY + (t & 1)), ((t - 2) >> 1) & 1)) { flags[1] = 1; break; }
-          tma_k(t, t & 1);
-          prefetch(t + kPrefetch);
-          ++nk;
-        }
-        const int tv = t - 1;
-        if (tv < ntiles) {
-          if (tv >= 2 && !mbar_wait(bar(BAR_V_EMPTY + (tv & 1)), ((tv - 2) >> 1) & 1)) {
-            flags[1] = 1;
-            break;
-          }
-          tma_v(tv, tv & 1);
-          ++nv;
-        }
+      int nk = ntiles > 1 ? 2 : 1;
+      for (int t = 2; t < ntiles && !flags[1]; ++t) {
+        if (!mbar_wait(bar(BAR_K_EMPTY + (t & 1)), ((t - 2) >> 1) & 1)) { flags[1] = 1; break; }
+        tma_k(t, t & 1);
+        prefetch(t + kPrefetch);
+        ++nk;
       }
       // no copy may still be in flight when the CTA leaves
       for (int st = 0; st < 2; ++st) {
-        const int ck = (nk - st + 1) / 2, cv = (nv - st + 1) / 2;  // loads into stage st
+        const int ck = (nk - st + 1) / 2;  // loads into stage st
         if (ck > 0) mbar_wait(bar(BAR_K_FULL + st), (ck - 1) & 1);
+      }
+    } else if (lane == 1) {
+      int nv = 1;
+      for (int tv = 1; tv < ntiles && !flags[1]; ++tv) {
+        if (tv >= 2 && !mbar_wait(bar(BAR_V_EMPTY + (tv & 1)), ((tv - 2) >> 1) & 1)) {
+          flags[1] = 1;
+          break;
+        }
+        tma_v(tv, tv & 1);
+        ++nv;
+      }
+      for (int st = 0; st < 2; ++st) {
+        const int cv = (nv - st + 1) / 2;
         if (cv > 0) mbar_wait(bar(BAR_V_FULL + st), (cv - 1) & 1);
       }
     }
@@ -258,18 +261,21 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
       const uint32_t idesc_qk = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
                                 ((uint32_t)(kKeys >> 4) << 24);
       const uint32_t idesc_pv = idesc_qk | (1u << 15) | (1u << 16);
-      const uint32_t qa = sbase + kOffQ, pta = sbase + L::off_pt;
+      // descriptor bases (built once): K stage 0, V stage 0, Q^T, P^T
+      const uint64_t kd0 = smem_desc(sbase + kOffK, 16, 1024);
+      const uint64_t vd0 = smem_desc(sbase + kOffV, kBox, 1024);
+      const uint64_t qd0 = smem_desc(sbase + kOffQ, 16, 1024);
+      const uint64_t ptd0 = smem_desc(sbase + L::off_pt, kBox, 1024);
       auto issue_qk = [&](int t) -> bool {
         const int st = t & 1;
         if (!mbar_wait(bar(BAR_K_FULL + st), (t >> 1) & 1)) return false;
         fence_after();
-        const uint32_t kb = sbase + kOffK + st * kTileBytes;
+        const uint64_t kd = kd0 + (uint64_t)(st * (kTileBytes >> 4));
+        mma_f16(tm_s[st], kd, qd0, idesc_qk, 0u);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t ad = smem_desc(kb + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc(qa + (kk >> 2) * (N * 128u) + (kk & 3) * 32, 16, 1024);
-          mma_f16(tm_s[st], ad, bd, idesc_qk, kk > 0);
-        }
+        for (int kk = 1; kk < kD / 16; ++kk)
+          mma_f16_acc(tm_s[st], kd + (((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
+                      qd0 + (((kk >> 2) * (N * 128u) + (kk & 3) * 32) >> 4), idesc_qk);
         mma_commit(bar(BAR_S_FULL + st));
         mma_commit(bar(BAR_K_EMPTY + st));
         return true;
@@ -280,13 +286,12 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
         if (!mbar_wait(bar(BAR_P_FULL), t & 1) || flags[1]) { ok = false; break; }
         if (!mbar_wait(bar(BAR_V_FULL + (t & 1)), (t >> 1) & 1)) { ok = false; break; }
         fence_after();
-        const uint32_t vb = sbase + kOffV + (t & 1) * kTileBytes;
+        const uint64_t vd = vd0 + (uint64_t)((t & 1) * (kTileBytes >> 4));
+        if (t == 0) mma_f16(tm_o, vd, ptd0, idesc_pv, 0u);
+        else mma_f16_acc(tm_o, vd, ptd0, idesc_pv);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t ad = smem_desc(vb + kk * 2048, kBox, 1024);
-          const uint64_t bd = smem_desc(pta + kk * 2048, kBox, 1024);
-          mma_f16(tm_o, ad, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < kKeys / 16; ++kk)
+          mma_f16_acc(tm_o, vd + 128 * kk, ptd0 + 128 * kk, idesc_pv);
         mma_commit(bar(BAR_PV_DONE));
         mma_commit(bar(BAR_V_EMPTY + (t & 1)));
       }
