@@ -268,6 +268,22 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def load_tensor_peak():
+    """Dense bf16 TF/s for a kernel timed alone (the burst figure)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def verify_flops(w, plen):
+    """Tensor-core work of the verify call: every packed row against every
+    prefix key, q.k over dk and p.v over dv (2 flops per multiply-add)."""
+    P = int(np.asarray(plen, dtype=np.int64).sum())
+    return 2.0 * w.R * w.Hq * P * (w.dk + w.dv)
+
+
 def load_traffic():
     """ncu DRAM bytes per launch, keyed by kernel, with the source digest they were taken at."""
     try:
@@ -401,6 +417,9 @@ def run_ours(args, dist):
     hbm_peak, peak_kind = load_peaks()
     dominant = max(("build", "verify", "accept"), key=lambda c: per_call[c])
     achieved = algo[dominant] / (per_call[dominant] / 1e3) / 1e9
+    # latent heads: the verify call is a dense contraction (about 2200 flop per
+    # byte of KV), so its roofline is the tensor pipe
+    tensor_bound = w.v_aliases_k and dominant == "verify"
     traffic = load_traffic().get(f"{args.config}:{dominant}")
     traffic_val = None
     if traffic and traffic.get("digest") == source_digest(CALL_SOURCES[dominant]):
@@ -434,6 +453,16 @@ def run_ours(args, dist):
         "device_err_word": err_word,
         "mean_accept_len": float(step.walk.accept_len.float().mean().item()),
     }
+    if tensor_bound:
+        tpeak, tkind = load_tensor_peak()
+        fl = verify_flops(w, host["plen"].numpy())
+        tf = fl / (per_call["verify"] / 1e3) / 1e12
+        line["roofline"] = {"kernel": "verify", "bound": "tensor", "achieved": round(tf, 1),
+                            "peak": tpeak, "unit": "TFLOP/s", "frac": round(tf / tpeak, 4),
+                            "peak_source": f"{tkind} (MEASURED_PEAKS.json bf16_tflops, burst)"
+                            if tkind == "measured" else "fallback 1.9 PF/s",
+                            "algorithmic_flops_per_launch": fl, "traffic": traffic_val,
+                            "algorithmic_bytes_per_launch": algo["verify"]}
     return line, w, host
 
 

@@ -31,16 +31,20 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-// Bounded wait for the phase with the given parity; false on timeout.
+// Bounded wait for the phase with the given parity; false on timeout.  Each
+// try_wait carries a suspend-time hint (in ns), so a waiting warp sleeps until
+// the phase completes instead of spinning on issue slots that the warps
+// sharing its scheduler need; the hint is far below the overall budget.
+constexpr uint32_t kSuspendHintNs = 1000000u;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   for (;;) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     if (ok) return true;
     if (clock64() - t0 > kWaitCycles) return false;
