@@ -118,6 +118,41 @@ tsd_status tsd_tree_build(const float* probs, int B, int S, int V, int k, int D,
                           size_t ws_bytes, int32_t* err, tsd_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * tsd_tree_build_adaptive
+ *
+ * The same tree with a per-request node count chosen by the cost-aware greedy
+ * rule ("Cost-Aware Diffusion Draft Trees", Method items 1, 3 and 4): nodes
+ * are taken in the best-first order of tsd_tree_build and node n+1 is kept
+ * only while it raises the expected throughput (1 + Phi(T)) / (C_d + C_v(|T|)),
+ * Phi being the sum of the kept nodes' scores (the expected number of
+ * accepted draft tokens); the first node that does not raise it ends the
+ * tree.  When C_v is convex and non-decreasing in the node count, the
+ * objective is unimodal and this stop is its maximum over 0..D_max.
+ * Arithmetic, fixed so that every implementation takes the same decision:
+ *   A_0 = 1, A_n = fp32(A_{n-1} + score_n);  cost_n = fp32(C_d + C_v(n));
+ *   keep node n+1  <=>  fp32(A_{n+1} * cost_n) > fp32(A_n * cost_{n+1}).
+ *
+ * cost_d   [B] fp32: drafting cost of the round (any time unit).
+ * cost_v   [B][1+D_max] fp32: verify cost with n = 0..D_max draft nodes at the
+ *          request's context length, in the same unit (for example from a
+ *          convex fit to measured step latencies).
+ * n_nodes  [B] int32 out: the kept count n* (0..D_max).
+ * Other arguments and outputs as tsd_tree_build with D = D_max; rows
+ * n*+1..D_max are inert padding (token -1, parent 0, depth 0, score 0,
+ * mask 0, is_leaf 0), which tsd_tree_verify_attn, tsd_accept_walk and
+ * tsd_commit_path accept and never take into the accepted path.  Leaves are
+ * computed over the kept rows only.
+ * ws: tsd_tree_build_workspace_size(B, S, V, k) bytes.
+ * -------------------------------------------------------------------------- */
+tsd_status tsd_tree_build_adaptive(const float* probs, int B, int S, int V, int k,
+                                   int D_max, const int32_t* root_tok,
+                                   const float* cost_d, const float* cost_v,
+                                   int32_t* token, int32_t* parent, int32_t* depth,
+                                   float* score, uint64_t* mask, uint8_t* is_leaf,
+                                   int32_t* n_nodes, void* ws, size_t ws_bytes,
+                                   int32_t* err, tsd_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * tsd_tree_verify_attn
  *
  * Branch-aware tree attention (V4 review, research gap item 1 and toy step 3).

@@ -111,6 +111,59 @@ def tree(top_p, top_id, D, root_tok, method="enum"):
     return out
 
 
+def adaptive_count(scores, cost_d, cost_v):
+    """Cost-aware node count ("Cost-Aware Diffusion Draft Trees for Speculative
+    Decoding", Method items 1, 3, 4): take the best-first nodes in order and
+    keep node n+1 only while it raises (1 + Phi) / (C_d + C_v(n)), Phi being
+    the sum of the kept scores; stop at the first node that does not.
+
+    scores: the D_max non-root scores of one request in row (pop) order;
+    cost_d: scalar; cost_v: [D_max + 1].  Every step is one fp32 operation,
+    in the order the C-ABI header fixes:
+      A_0 = 1, A_{n+1} = A_n + s_{n+1}, cost_n = C_d + C_v(n),
+      keep n+1 iff (A_{n+1} * cost_n) > (A_n * cost_{n+1}).
+    """
+    f = np.float32
+    A = f(1.0)
+    cd = f(cost_d)
+    cost = [f(cd + f(c)) for c in np.asarray(cost_v, np.float32)]
+    n = 0
+    for s in np.asarray(scores, np.float32):
+        A1 = f(A + s)
+        if not f(A1 * cost[n]) > f(A * cost[n + 1]):
+            break
+        A = A1
+        n += 1
+    return n
+
+
+def tree_adaptive(top_p, top_id, D_max, root_tok, cost_d, cost_v, method="enum"):
+    """The best-first tree of tree() with each request's node count chosen by
+    adaptive_count; rows past the count are inert padding (token -1, parent 0,
+    depth 0, score 0, mask 0, not a leaf) and leaves are recomputed over the
+    kept rows.  Returns tree() arrays plus n_nodes [B]."""
+    t = tree(top_p, top_id, D_max, root_tok, method)
+    cost_d = np.asarray(cost_d, np.float32)
+    cost_v = np.asarray(cost_v, np.float32)
+    B = t["token"].shape[0]
+    n_nodes = np.zeros(B, np.int32)
+    for b in range(B):
+        n = adaptive_count(t["score"][b, 1:], cost_d[b], cost_v[b])
+        n_nodes[b] = n
+        t["token"][b, n + 1:] = -1
+        t["parent"][b, n + 1:] = 0
+        t["depth"][b, n + 1:] = 0
+        t["score"][b, n + 1:] = 0.0
+        t["mask"][b, n + 1:] = 0
+        leaf = np.ones(D_max + 1, np.uint8)
+        for r in range(1, n + 1):
+            leaf[t["parent"][b, r]] = 0
+        leaf[n + 1:] = 0
+        t["is_leaf"][b] = leaf
+    t["n_nodes"] = n_nodes
+    return t
+
+
 def verify_attn(q, kcache, vcache, prefix_len, ktree, vtree, mask, scale,
                 v_aliases_k=False, dv=None, sel=None, nthreads=0):
     """fp64 tree-verify attention.

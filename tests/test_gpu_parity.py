@@ -546,3 +546,100 @@ def test_verify_ignores_nonfinite_cache_rows_past_prefix(name, force, monkeypatc
         if vc is not None:
             vc[b, :, p:] = float("nan")
     check_attention(w, q, kc, vc, plen, kt, vt, d["tree"]["mask"])
+
+
+# --------------------------------------------- cost-aware adaptive budget --
+
+def _cost_tables(w, kind, seed=0):
+    """Convex, non-decreasing verify costs (same unit as the drafting cost)
+    placing the stop inside, below or above the budget."""
+    rng = np.random.default_rng(seed)
+    n = np.arange(w.D + 1, dtype=np.float64)
+    if kind == "mid":
+        cd = rng.uniform(5, 15, w.B)
+        cv = np.stack([20 + rng.uniform(0.5, 3) * n + rng.uniform(0, 0.3) * n * n
+                       for _ in range(w.B)])
+    elif kind == "none":
+        cd, cv = np.full(w.B, 1.0), np.stack([1.0 + 1e9 * (n > 0)] * w.B)
+    else:  # "all": free nodes
+        cd, cv = np.full(w.B, 10.0), np.full((w.B, w.D + 1), 5.0)
+    return cd.astype(np.float32), cv.astype(np.float32)
+
+
+def run_adaptive(step, probs, root, cd, cv):
+    p, r, c1, c2 = gpu(probs, root, torch.from_numpy(cd), torch.from_numpy(cv))
+    step.build_adaptive(p, r, c1, c2)
+    torch.cuda.synchronize()
+    t = step.tree
+    got = dict(token=t.token.cpu().numpy(), parent=t.parent.cpu().numpy(),
+               depth=t.depth.cpu().numpy(), score=t.score.cpu().numpy(),
+               mask=t.mask.cpu().numpy().view(np.uint64), is_leaf=t.is_leaf.cpu().numpy())
+    return got, step.n_nodes.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["toy", "qwen", "batched", "long", "mla"])
+@pytest.mark.parametrize("kind", ["mid", "none", "all"])
+def test_tree_build_adaptive_matches_oracle(name, kind):
+    d = inputs(name)
+    w = d["w"]
+    cd, cv = _cost_tables(w, kind, seed=len(name))
+    ref = oracle.tree_adaptive(d["tp"], d["ti"], w.D, d["root"].numpy(), cd, cv, method="beam")
+    step = TreeVerifyStep.for_workload(w, DEV)
+    got, n = run_adaptive(step, d["probs"], d["root"], cd, cv)
+    np.testing.assert_array_equal(n, ref["n_nodes"])
+    assert_tree_equal(got, ref)
+    if kind == "none":
+        assert (n == 0).all()
+    if kind == "all":   # free nodes: stops only where fp32 1 + Phi stops growing
+        assert (n >= min(w.D, 4)).all()
+
+
+def test_adaptive_step_never_accepts_padding():
+    """Verify, walk and commit on a tree with padded rows: the walk equals the
+    oracle's on the padded tree and stays within the kept rows."""
+    d = inputs("batched", B=6, P=700, P_min=100, V=3000)
+    w = d["w"]
+    cd, cv = _cost_tables(w, "mid", seed=11)
+    ref = oracle.tree_adaptive(d["tp"], d["ti"], w.D, d["root"].numpy(), cd, cv, method="beam")
+    step = TreeVerifyStep.for_workload(w, DEV)
+    got, n = run_adaptive(step, d["probs"], d["root"], cd, cv)
+    assert_tree_equal(got, ref)
+    # target logits that favour the draft: most walks go deep
+    tl = W.target_logits(w, torch.from_numpy(ref["depth"]), d["logits"])
+    tgt = oracle.argmax(tl.numpy())
+    ref_walk = oracle.accept_walk(tgt, ref, w.S)
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    g = gpu(q, kc, vc, plen, kt, vt, tl)
+    step.verify(*g[:6])
+    step.accept(g[6])
+    step.commit(g[4], g[5], g[1], g[2], g[3])
+    torch.cuda.synchronize()
+    wk = step.walk
+    for key in ("accept_len", "accept_rows", "bonus", "chain_id"):
+        np.testing.assert_array_equal(getattr(wk, key).cpu().numpy(), ref_walk[key])
+    rows = wk.accept_rows.cpu().numpy()
+    for b in range(w.B):
+        L = int(wk.accept_len[b])
+        assert all(1 <= rows[b, i] <= n[b] for i in range(1, L + 1))
+    assert int(step.err[0]) == 0
+
+
+def test_cost_model_calibrated_on_this_gpu():
+    """Measure the step at a few budgets and prefix lengths, fit the convex
+    model and drive the adaptive build with it."""
+    pytest.importorskip("scipy")
+    from tree_speculative_decoding_tsd_gb300 import costmodel
+    w = W.WORKLOADS["qwen"].scaled(V=20000)
+    cost_d, samples = costmodel.measure(w, [2, 8, 32], [512, 4096], steps=5, warmup=2, device=DEV)
+    assert cost_d > 0
+    m = costmodel.CostModel.from_samples(cost_d, samples)
+    cv = m.verify_cost(2048, 32).astype(np.float64)
+    assert np.all(np.diff(cv) >= -1e-3) and np.all(np.diff(cv, 2) >= -1e-3)
+    d = inputs("qwen", D=32, V=20000)
+    wq = d["w"]
+    cdt, cvt = m.tables([2048] * wq.B, wq.D)
+    ref = oracle.tree_adaptive(d["tp"], d["ti"], wq.D, d["root"].numpy(), cdt, cvt, method="beam")
+    step = TreeVerifyStep.for_workload(wq, DEV)
+    got, n = run_adaptive(step, d["probs"], d["root"], cdt, cvt)
+    np.testing.assert_array_equal(n, ref["n_nodes"])
+    assert_tree_equal(got, ref)

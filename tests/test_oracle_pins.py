@@ -421,3 +421,63 @@ def test_commit_capacity_overflow_is_skipped():
     np.testing.assert_array_equal(vc[1, :, 3:5], vt[1, [0, 2]].transpose(1, 0, 2))
     np.testing.assert_array_equal(kc[1, :, :3], kc0[1, :, :3])
     np.testing.assert_array_equal(kc[1, :, 5:], kc0[1, :, 5:])
+
+
+# ------------------------------------------------- cost-aware node count --
+# "Cost-Aware Diffusion Draft Trees for Speculative Decoding", Method 1, 3, 4:
+# keep adding best-first nodes while (1 + Phi) / (C_d + C_v(n)) rises.
+
+def test_adaptive_toy_tree_with_linear_cost():
+    """The page's toy tree (scores 0.5, 0.375, 0.3125 in best-first order) with
+    C_d = 1 and C_v(n) = n / 4: the objective is 1, 1.2, 1.25, 1.25 for
+    n = 0..3, so nodes 1 and 2 raise it and node 3 does not (all values exact
+    binary fractions): two nodes are kept, and row 3 becomes padding."""
+    tp = np.array([[[0.5, 0.375], [0.625, 0.25]]], np.float32)
+    ti = np.array([[[1, 2], [1, 0]]], np.int32)
+    t = oracle.tree_adaptive(tp, ti, 3, np.array([0], np.int32), [1.0], [[0.0, 0.25, 0.5, 0.75]])
+    assert t["n_nodes"].tolist() == [2]
+    assert t["token"][0].tolist() == [0, 1, 2, -1]
+    assert t["parent"][0].tolist() == [-1, 0, 0, 0]
+    assert t["mask"][0].tolist() == [0, 1, 2, 0]
+    assert t["is_leaf"][0].tolist() == [0, 1, 1, 0]
+    # a cheaper node lets the third one in
+    t = oracle.tree_adaptive(tp, ti, 3, np.array([0], np.int32), [1.0], [[0.0, 0.25, 0.5, 0.7]])
+    assert t["n_nodes"].tolist() == [3]
+
+
+def _objective(scores, cost_d, cost_v, n):
+    return (1.0 + float(np.sum(np.asarray(scores[:n], np.float64)))) / (cost_d + float(cost_v[n]))
+
+
+def test_adaptive_stop_is_the_argmax_under_convex_cost():
+    """Unimodality (Method 3): with non-increasing scores and a convex,
+    non-decreasing verify cost, the first non-improving node is the global
+    maximum of the objective over n = 0..D (checked against an fp64 brute
+    force wherever the maximum is clear of rounding)."""
+    rng = np.random.default_rng(3)
+    checked = 0
+    for _ in range(400):
+        D = int(rng.integers(1, 40))
+        s = np.sort(rng.uniform(0.0, 1.0, D) ** rng.uniform(1, 4))[::-1].astype(np.float32)
+        a, b, c = rng.uniform(1, 50), rng.uniform(0, 3), rng.uniform(0, 0.2)
+        n = np.arange(D + 1)
+        cv = (a + b * n + c * n * n).astype(np.float32)
+        cd = np.float32(rng.uniform(1, 100))
+        J = np.array([_objective(s, float(cd), cv, m) for m in range(D + 1)])
+        best = int(np.argmax(J))
+        srt = np.sort(J)
+        if D > 0 and srt[-1] - srt[-2] < 1e-5 * srt[-1]:
+            continue
+        assert oracle.adaptive_count(s, cd, cv) == best
+        checked += 1
+    assert checked > 300
+
+
+def test_adaptive_extremes():
+    s = np.array([0.5, 0.25, 0.125, 0.0625], np.float32)
+    # no marginal verify cost: every node with a positive score helps
+    assert oracle.adaptive_count(s, 10.0, np.full(5, 3.0, np.float32)) == 4
+    # the first node alone costs more than it can ever return
+    assert oracle.adaptive_count(s, 1.0, np.array([0, 1e9, 1e9, 1e9, 1e9], np.float32)) == 0
+    # zero-probability nodes never raise the objective
+    assert oracle.adaptive_count(np.zeros(4, np.float32), 1.0, np.arange(5, dtype=np.float32)) == 0

@@ -18,6 +18,10 @@
 //    (children are the top-k of the next position in rank order, so a node's
 //    first child and younger siblings never precede it); this visits nodes in
 //    exactly the total order (score desc, depth asc, rank tuple asc).
+//    With a cost table (tsd_tree_build_adaptive) the pops stop early: the
+//    greedy rule of "Cost-Aware Diffusion Draft Trees", Method items 1, 3-4,
+//    adds the next node only while it raises the throughput objective
+//    (1 + Phi) / (C_d + C_v(n)), Phi being the sum of the kept scores.
 #include "tsd_common.cuh"
 #include "tsd_host.h"
 #include "tsd_scan.cuh"
@@ -32,6 +36,7 @@ constexpr int kMaxD = 64;
 struct TreeSmem {
   float tp[kMaxS][kMaxK];     // top-k probabilities per position
   int32_t ti[kMaxS][kMaxK];   // top-k token ids per position
+  float cost[kMaxD + 1];      // adaptive mode: C_d + C_v(n), n = 0..D
   uint8_t has_child[kMaxD + 1];
 };
 
@@ -83,12 +88,18 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
                        const int32_t* __restrict__ root_tok, int32_t* __restrict__ token,
                        int32_t* __restrict__ parent, int32_t* __restrict__ depth,
                        float* __restrict__ score, uint64_t* __restrict__ mask,
-                       uint8_t* __restrict__ is_leaf) {
+                       uint8_t* __restrict__ is_leaf, const float* __restrict__ cost_d,
+                       const float* __restrict__ cost_v, int32_t* __restrict__ n_nodes) {
   __shared__ TreeSmem s;
   const int b = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = D + 1;
   const long o = (long)b * R;
+  const bool adaptive = cost_v != nullptr;
+  // adaptive mode: round cost of a tree with n nodes, fp32 C_d + C_v(n)
+  if (adaptive)
+    for (int n = threadIdx.x; n <= D; n += blockDim.x)
+      s.cost[n] = __fadd_rn(cost_d[b], cost_v[(long)b * R + n]);
 
   // ---- warp p merges the chunk lists of position p into its top-k ----
   // (at most kScanMaxCand candidates: every lane loads its share up front)
@@ -132,6 +143,11 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
     f_key[0] = primary_key(f_sc[0], 1, 0ull);
   }
   int nf = 1;
+  // Phi accumulation for the adaptive stop: A = 1 + Phi(first n nodes), fp32
+  // in pop order.  Node n+1 is kept iff (A + s) * cost[n] > A * cost[n+1]
+  // (fp32 products, i.e. the objective rises); the first failure ends the tree.
+  float acc = 1.0f;
+  int kept = D;
 
   for (int row = 1; row <= D; ++row) {
     // this lane's smallest primary key, then the warp's: high word (score),
@@ -180,6 +196,14 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
     }
     // the popped entry and the new row
     const float sc = bcast(f_sc, best), psc = bcast(f_psc, best);
+    if (adaptive) {
+      const float acc1 = __fadd_rn(acc, sc);
+      if (!(__fmul_rn(acc1, s.cost[row - 1]) > __fmul_rn(acc, s.cost[row]))) {
+        kept = row - 1;
+        break;
+      }
+      acc = acc1;
+    }
     const int d = bcast(f_d, best), par = bcast(f_par, best), rk = bcast(f_rk, best);
     const uint64_t w0 = bcast(f_w0, best), w1 = bcast(f_w1, best);
     const uint64_t pm = bcast(f_pm, best);
@@ -226,26 +250,37 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   }
 
   // ---- leaves and outputs (each lane writes its own rows) ----
+  // Rows past the kept count (adaptive mode only) are inert padding: token -1
+  // (no target token matches it), parent 0, depth 0, score 0, mask 0, not a
+  // leaf, so verify, walk and commit treat them as never accepted.
   for (int r = lane; r <= D; r += 32) s.has_child[r] = 0;
   __syncwarp();
 #pragma unroll
   for (int j = 0; j < kSlots; ++j) {
     const int r = lane + 32 * j;
-    if (r >= 1 && r <= D) s.has_child[r_par[j]] = 1;
+    if (r >= 1 && r <= kept) s.has_child[r_par[j]] = 1;
   }
   __syncwarp();
 #pragma unroll
   for (int j = 0; j < kSlots; ++j) {
     const int r = lane + 32 * j;
-    if (r <= D) {
+    if (r <= kept) {
       token[o + r] = r_tok[j];
       parent[o + r] = r_par[j];
       depth[o + r] = r_dep[j];
       score[o + r] = r_sc[j];
       mask[o + r] = r_mask[j];
       is_leaf[o + r] = s.has_child[r] ? 0 : 1;
+    } else if (r <= D) {
+      token[o + r] = -1;
+      parent[o + r] = 0;
+      depth[o + r] = 0;
+      score[o + r] = 0.f;
+      mask[o + r] = 0ull;
+      is_leaf[o + r] = 0;
     }
   }
+  if (n_nodes != nullptr && lane == 0) n_nodes[b] = kept;
 }
 
 }  // namespace
@@ -259,12 +294,13 @@ extern "C" size_t tsd_tree_build_workspace_size(int B, int S, int V, int k) {
   return (size_t)B * S * g.nchunk * k * sizeof(uint64_t);
 }
 
-extern "C" tsd_status tsd_tree_build(const float* probs, int B, int S, int V, int k, int D,
-                                     const int32_t* root_tok, int32_t* token, int32_t* parent,
-                                     int32_t* depth, float* score, uint64_t* mask,
-                                     uint8_t* is_leaf, void* ws, size_t ws_bytes, int32_t* err,
-                                     tsd_stream_t stream) {
-  (void)err;
+namespace {
+
+tsd_status tree_build_impl(const float* probs, int B, int S, int V, int k, int D,
+                           const int32_t* root_tok, const float* cost_d, const float* cost_v,
+                           int32_t* token, int32_t* parent, int32_t* depth, float* score,
+                           uint64_t* mask, uint8_t* is_leaf, int32_t* n_nodes, void* ws,
+                           size_t ws_bytes, tsd_stream_t stream) {
   if (B < 1 || S < 1 || S > kMaxS || k < 1 || k > kMaxK || V < k || D < 1 || D > kMaxD)
     return TSD_ERR_INVALID_ARG;
   if (tree_node_count(S, k) < D) return TSD_ERR_INVALID_ARG;
@@ -282,6 +318,32 @@ extern "C" tsd_status tsd_tree_build(const float* probs, int B, int S, int V, in
   vocab_scan_kernel<false><<<(unsigned)ctas, kScanThreads, 0, st>>>(probs, V, k, g.nchunk,
                                                                     g.chunk_len, part);
   best_first_tree_kernel<<<B, 32 * S, 0, st>>>(part, S, k, D, g.nchunk, root_tok, token, parent,
-                                           depth, score, mask, is_leaf);
+                                               depth, score, mask, is_leaf, cost_d, cost_v,
+                                               n_nodes);
   return cuda_status();
+}
+
+}  // namespace
+
+extern "C" tsd_status tsd_tree_build(const float* probs, int B, int S, int V, int k, int D,
+                                     const int32_t* root_tok, int32_t* token, int32_t* parent,
+                                     int32_t* depth, float* score, uint64_t* mask,
+                                     uint8_t* is_leaf, void* ws, size_t ws_bytes, int32_t* err,
+                                     tsd_stream_t stream) {
+  (void)err;
+  return tree_build_impl(probs, B, S, V, k, D, root_tok, nullptr, nullptr, token, parent, depth,
+                         score, mask, is_leaf, nullptr, ws, ws_bytes, stream);
+}
+
+extern "C" tsd_status tsd_tree_build_adaptive(const float* probs, int B, int S, int V, int k,
+                                              int D_max, const int32_t* root_tok,
+                                              const float* cost_d, const float* cost_v,
+                                              int32_t* token, int32_t* parent, int32_t* depth,
+                                              float* score, uint64_t* mask, uint8_t* is_leaf,
+                                              int32_t* n_nodes, void* ws, size_t ws_bytes,
+                                              int32_t* err, tsd_stream_t stream) {
+  (void)err;
+  if (!ok_ptr(cost_d) || !ok_ptr(cost_v) || !ok_ptr(n_nodes)) return TSD_ERR_INVALID_ARG;
+  return tree_build_impl(probs, B, S, V, k, D_max, root_tok, cost_d, cost_v, token, parent, depth,
+                         score, mask, is_leaf, n_nodes, ws, ws_bytes, stream);
 }

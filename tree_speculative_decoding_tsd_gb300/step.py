@@ -13,8 +13,8 @@ import dataclasses
 import torch
 
 from . import (make_desc, tsd_accept_walk, tsd_accept_walk_workspace_size, tsd_commit_path,
-               tsd_tree_build, tsd_tree_build_workspace_size, tsd_tree_verify_attn,
-               tsd_verify_workspace_size, workspace)
+               tsd_tree_build, tsd_tree_build_adaptive, tsd_tree_build_workspace_size,
+               tsd_tree_verify_attn, tsd_verify_workspace_size, workspace)
 
 
 @dataclasses.dataclass
@@ -60,6 +60,7 @@ class TreeVerifyStep:
             accept_rows=torch.empty((B, S + 1), **i32), bonus=torch.empty((B,), **i32),
             chain_id=torch.empty((B,), **i32))
         self.err = torch.zeros((4,), **i32)
+        self.n_nodes = torch.zeros((B,), **i32)
         self.ws_build = workspace(tsd_tree_build_workspace_size(B, S, V, k), dev)
         self.ws_verify = workspace(tsd_verify_workspace_size(self.desc), dev)
         self.ws_walk = workspace(tsd_accept_walk_workspace_size(B, D, V), dev)
@@ -69,6 +70,14 @@ class TreeVerifyStep:
         t = self.tree
         tsd_tree_build(probs, self.k, self.D, root_tok, t.token, t.parent, t.depth, t.score,
                        t.mask, t.is_leaf, self.ws_build, self.err, stream)
+
+    def build_adaptive(self, probs, root_tok, cost_d, cost_v, stream=None):
+        """Tree with the cost-aware node count per request (at most D); the
+        kept counts land in ``self.n_nodes``, the remaining rows are padding."""
+        t = self.tree
+        tsd_tree_build_adaptive(probs, self.k, self.D, root_tok, cost_d, cost_v, t.token, t.parent,
+                                t.depth, t.score, t.mask, t.is_leaf, self.n_nodes, self.ws_build,
+                                self.err, stream)
 
     def verify(self, q, kcache, vcache, prefix_len, ktree, vtree, stream=None):
         tsd_tree_verify_attn(self.desc, q, kcache, vcache, prefix_len, ktree, vtree,
