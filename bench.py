@@ -304,6 +304,7 @@ def source_digest(files):
 
 CALL_SOURCES = {
     "build": ["tsd_tree_build.cu", "tsd_scan.cuh", "tsd_common.cuh"],
+    "build_conditioned": ["tsd_tree_cond.cu", "tsd_common.cuh"],
     "verify": ["tsd_verify.cu", "tsd_verify_tc.cu", "tsd_verify_mla.cu", "tsd_verify_mma.cu",
                "tsd_verify.cuh", "tsd_tcgen05.cuh", "tsd_common.cuh"],
     "accept": ["tsd_accept.cu", "tsd_scan.cuh", "tsd_common.cuh"],
@@ -411,6 +412,9 @@ def run_ours(args, dist):
     # ---- e2e: host buffers through the Python API ----
     e2e = run_e2e(args, step, host, d, dev, stream, plen0)
 
+    # ---- cost-aware adaptive budget (tsd_tree_build_adaptive) ----
+    adaptive = run_adaptive(args, w, step, d, dev, stream)
+
     nodes = w.B * w.D
     value = nodes * dist.world / (ms / 1e3)
     algo, kv_bytes = algorithmic_bytes(w, host["plen"].numpy())
@@ -452,6 +456,7 @@ def run_ours(args, dist):
         "wall_s_timed_region": round(t_wall, 4),
         "device_err_word": err_word,
         "mean_accept_len": float(step.walk.accept_len.float().mean().item()),
+        "adaptive": adaptive,
     }
     if tensor_bound:
         tpeak, tkind = load_tensor_peak()
@@ -464,6 +469,42 @@ def run_ours(args, dist):
                             "algorithmic_flops_per_launch": fl, "traffic": traffic_val,
                             "algorithmic_bytes_per_launch": algo["verify"]}
     return line, w, host
+
+
+def run_adaptive(args, w, step, d, dev, stream):
+    """Cost model fitted to this GPU's own step latencies at budgets D/4, D/2, D
+    (convex, non-decreasing in n), then tsd_tree_build_adaptive timed per call
+    with CUDA events; reports the per-call time and the kept node counts."""
+    size = w.B * w.cap * w.Hkv * (w.dk + (0 if w.v_aliases_k else w.dv))
+    if size > 2e8:
+        return {"skipped": "synthetic inputs for the calibration sweep too large to generate "
+                           "in the default run"}
+    try:
+        from tree_speculative_decoding_tsd_gb300 import costmodel
+        ell = int(np.mean(W.prefix_lens(w).numpy()))
+        budgets = sorted({max(1, w.D // 4), max(1, w.D // 2), w.D})
+        cost_d, samples = costmodel.measure(w, budgets, [ell], steps=5, warmup=2, device=dev)
+        model = costmodel.CostModel.from_samples(cost_d, samples)
+    except ImportError as e:
+        return {"skipped": f"cost fit unavailable: {e}"}
+    cd, cv = model.tables([ell] * w.B, w.D)
+    cd, cv = torch.from_numpy(cd).to(dev), torch.from_numpy(cv).to(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step.build_adaptive(d["probs"], d["root"], cd, cv, stream)
+        for a, b in ev:
+            a.record(stream)
+            step.build_adaptive(d["probs"], d["root"], cd, cv, stream)
+            b.record(stream)
+    torch.cuda.synchronize(dev)
+    n = step.n_nodes.cpu().numpy()
+    return {"build_adaptive_us": round(statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3, 2),
+            "mean_nodes": float(n.mean()), "min_nodes": int(n.min()), "max_nodes": int(n.max()),
+            "D_max": w.D, "cost_model": {"cost_d_us": round(cost_d, 2), "prefix_len": ell,
+                                         "budgets": budgets,
+                                         "verify_side_us": [round(x, 2) for x in samples[ell][1]]}}
 
 
 def run_e2e(args, step, host, d, dev, stream, plen0):

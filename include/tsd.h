@@ -153,6 +153,37 @@ tsd_status tsd_tree_build_adaptive(const float* probs, int B, int S, int V, int 
                                    int32_t* err, tsd_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * tsd_tree_build_conditioned
+ *
+ * The best-first tree over a caller-given candidate forest whose proposals are
+ * conditioned on their parent node (EAGLE-style drafting: each node's children
+ * are the drafter's proposals at that node), as in the V4 review's toy example
+ * ("How it works" steps 1-2: B proposes B and C, C proposes A and B; the
+ * expanded tree is pruned to the D nodes of highest cumulative score), with
+ * the greedy best-first choice of "Cost-Aware Diffusion Draft Trees", Method
+ * item 2.
+ *
+ * cand_p      [B][C] fp32 in [0, 1]: probability of candidate c given its parent
+ * cand_tok    [B][C] int32: token of candidate c
+ * cand_parent [B][C] int32: index of c's parent candidate (< c), or -1 for a
+ *             child of the root (candidates are listed parents first)
+ * Score of a candidate: fp32 product of cand_p along its path, in depth order
+ * (1.0 for the root).  Rows 1..D are the first D candidates in the order
+ * (score desc, depth asc, candidate index asc), which lists parents before
+ * children; outputs as tsd_tree_build.  Limits: 1 <= C <= 2048, 1 <= D <=
+ * min(64, C).  A forest with a parent index out of range, a probability outside
+ * [0, 1] (or NaN), or fewer than D candidates within depth 65 sets
+ * TSD_DEV_ERR_BAD_TREE | b in err and gives request b a root-only tree (rows
+ * 1..D inert padding: token -1, parent 0, depth 0, score 0, mask 0, not leaf).
+ * -------------------------------------------------------------------------- */
+tsd_status tsd_tree_build_conditioned(const float* cand_p, const int32_t* cand_tok,
+                                      const int32_t* cand_parent, int B, int C, int D,
+                                      const int32_t* root_tok, int32_t* token,
+                                      int32_t* parent, int32_t* depth, float* score,
+                                      uint64_t* mask, uint8_t* is_leaf, int32_t* err,
+                                      tsd_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * tsd_tree_verify_attn
  *
  * Branch-aware tree attention (V4 review, research gap item 1 and toy step 3).

@@ -164,6 +164,72 @@ def tree_adaptive(top_p, top_id, D_max, root_tok, cost_d, cost_v, method="enum")
     return t
 
 
+def tree_conditioned(cand_p, cand_tok, cand_parent, D, root_tok):
+    """Best-first tree over a forest of parent-conditioned proposals (the V4
+    review's toy, "How it works" steps 1-2: each node's children are that
+    node's own proposals; the tree keeps the D nodes of highest cumulative
+    score; "Cost-Aware Diffusion Draft Trees", Method 2).
+
+    cand_p/cand_tok/cand_parent: [B][C], parents listed first (parent < c, -1
+    for a child of the root).  Score: fp32 product along the path in depth
+    order.  Rows 1..D: the first D candidates by (score desc, depth asc, index
+    asc) among those within depth 65.  A malformed forest (parent out of range,
+    probability outside [0, 1], too few candidates) gives a root-only tree with
+    padding rows and status 1 for that request.  Returns tree() arrays plus
+    "status" [B].
+    """
+    f = np.float32
+    cand_p = np.asarray(cand_p, np.float32)
+    cand_tok = np.asarray(cand_tok, np.int32)
+    cand_parent = np.asarray(cand_parent, np.int32)
+    B, C = cand_p.shape
+    R = D + 1
+    out = dict(token=np.zeros((B, R), np.int32), parent=np.zeros((B, R), np.int32),
+               depth=np.zeros((B, R), np.int32), score=np.zeros((B, R), np.float32),
+               mask=np.zeros((B, R), np.uint64), is_leaf=np.zeros((B, R), np.uint8),
+               status=np.zeros(B, np.int32))
+    for b in range(B):
+        sc = [f(0)] * C
+        dep = [0] * C
+        bad = False
+        for c in range(C):
+            pp, p = int(cand_parent[b, c]), cand_p[b, c]
+            if pp < -1 or pp >= c or not (0.0 <= p <= 1.0):
+                bad = True
+                break
+            sc[c] = f(f(1.0) * p) if pp < 0 else f(sc[pp] * p)
+            dep[c] = 1 if pp < 0 else dep[pp] + 1
+        order = sorted((c for c in range(C) if not bad and dep[c] <= 65),
+                       key=lambda c: (-float(sc[c]), dep[c], c))
+        if bad or len(order) < D:
+            bad = True
+        out["token"][b, 0] = root_tok[b]
+        out["parent"][b, 0] = -1
+        out["score"][b, 0] = 1.0
+        if bad:
+            out["status"][b] = 1
+            out["token"][b, 1:] = -1
+            out["is_leaf"][b, 0] = 1
+            continue
+        row_of = {}
+        masks = [0] * R
+        has_child = [False] * R
+        for i, c in enumerate(order[:D], start=1):
+            row_of[c] = i
+            pp = int(cand_parent[b, c])
+            pr = 0 if pp < 0 else row_of[pp]   # a kept node's parent is kept earlier
+            masks[i] = masks[pr] | (1 << (i - 1))
+            has_child[pr] = True
+            out["token"][b, i] = cand_tok[b, c]
+            out["parent"][b, i] = pr
+            out["depth"][b, i] = dep[c]
+            out["score"][b, i] = sc[c]
+            out["mask"][b, i] = masks[i]
+        for i in range(R):
+            out["is_leaf"][b, i] = 0 if has_child[i] else 1
+    return out
+
+
 def verify_attn(q, kcache, vcache, prefix_len, ktree, vtree, mask, scale,
                 v_aliases_k=False, dv=None, sel=None, nthreads=0):
     """fp64 tree-verify attention.

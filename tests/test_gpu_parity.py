@@ -459,6 +459,15 @@ def test_verify_each_path_reduced(force_path, key):
     check_attention(w, *attn_inputs(w), d["tree"]["mask"])
 
 
+@pytest.mark.parametrize("force_path", ["tc"], indirect=True)
+@pytest.mark.parametrize("D", [3, 5, 7, 11])
+def test_verify_tcgen05_small_trees(force_path, D):
+    """Packed-row counts 16..48 (g = 4): MMA N of 16, 32 and 48."""
+    d = inputs("qwen", D=D, P=1300, P_min=1300, V=3000)
+    w = d["w"]
+    check_attention(w, *attn_inputs(w), d["tree"]["mask"])
+
+
 @pytest.mark.parametrize("force_path", ["tc", "mma"], indirect=True)
 @pytest.mark.parametrize("D", [15, 19, 23, 27, 31, 35, 48])
 def test_verify_tensor_core_column_tiles(force_path, D):
@@ -643,3 +652,134 @@ def test_cost_model_calibrated_on_this_gpu():
     got, n = run_adaptive(step, d["probs"], d["root"], cdt, cvt)
     np.testing.assert_array_equal(n, ref["n_nodes"])
     assert_tree_equal(got, ref)
+
+
+# ------------------------------------------------ one graph per round --
+
+@pytest.mark.parametrize("adaptive", [False, True])
+def test_captured_round_matches_eager_calls(adaptive):
+    """The whole round recorded as one CUDA graph gives bit-identical trees,
+    attention, walk and committed cache to the eager calls, replay after
+    replay (inputs refilled in place between replays)."""
+    d = inputs("batched", B=4, P=600, P_min=200, V=4000)
+    w, tree = d["w"], d["tree"]
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    tl = W.target_logits(w, torch.from_numpy(tree["depth"]), d["logits"])
+    cd, cv = _cost_tables(w, "mid", seed=2) if adaptive else (None, None)
+    extra = (torch.from_numpy(cd).to(DEV), torch.from_numpy(cv).to(DEV)) if adaptive else (None, None)
+
+    def fresh():
+        return gpu(d["probs"], d["root"], q, kc.clone(), None if vc is None else vc.clone(),
+                   plen.clone(), kt, vt, tl)
+
+    eager = TreeVerifyStep.for_workload(w, DEV)
+    ge = fresh()
+    eager._round(*ge, *extra, None)
+    torch.cuda.synchronize()
+
+    graphed = TreeVerifyStep.for_workload(w, DEV)
+    gg = fresh()
+    g = graphed.capture(*gg, *extra)
+    for _ in range(2):
+        # restore the state the eager round started from, then replay
+        gg[3].copy_(kc.to(DEV))
+        if vc is not None:
+            gg[4].copy_(vc.to(DEV))
+        gg[5].copy_(plen.to(DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        for f in ("token", "parent", "depth", "score", "mask", "is_leaf"):
+            assert torch.equal(getattr(eager.tree, f), getattr(graphed.tree, f)), f
+        assert torch.equal(eager.out, graphed.out) and torch.equal(eager.lse, graphed.lse)
+        for f in ("tgt", "accept_len", "accept_rows", "bonus", "chain_id"):
+            assert torch.equal(getattr(eager.walk, f), getattr(graphed.walk, f)), f
+        assert torch.equal(ge[3], gg[3]) and torch.equal(ge[5], gg[5])
+        if vc is not None:
+            assert torch.equal(ge[4], gg[4])
+        if adaptive:
+            assert torch.equal(eager.n_nodes, graphed.n_nodes)
+    assert int(graphed.err[0]) == 0
+
+
+# ------------------------------------------- parent-conditioned proposals --
+
+def _random_forest(B, C, seed, quant=None):
+    """Random parents (any earlier candidate or the root), skewed probabilities."""
+    rng = np.random.default_rng(seed)
+    par = np.full((B, C), -1, np.int32)
+    for b in range(B):
+        for c in range(1, C):
+            par[b, c] = int(rng.integers(-1, c))
+    p = rng.uniform(0.0, 1.0, (B, C)) ** rng.uniform(1, 3)
+    if quant:
+        p = np.round(p * quant) / quant
+    tok = rng.integers(0, 50000, (B, C)).astype(np.int32)
+    return p.astype(np.float32), tok, par
+
+
+def run_conditioned(w, cp, ct, cpar, root, D):
+    step = TreeVerifyStep(w.B, w.S, w.V, w.k, D, w.Hq, w.Hkv, w.dk, w.dv, w.cap, w.torch_dtype,
+                          w.v_aliases_k, w.scale, DEV)
+    g = gpu(torch.from_numpy(cp), torch.from_numpy(ct), torch.from_numpy(cpar), root)
+    step.err.zero_()
+    step.build_conditioned(*g)
+    torch.cuda.synchronize()
+    t = step.tree
+    got = dict(token=t.token.cpu().numpy(), parent=t.parent.cpu().numpy(),
+               depth=t.depth.cpu().numpy(), score=t.score.cpu().numpy(),
+               mask=t.mask.cpu().numpy().view(np.uint64), is_leaf=t.is_leaf.cpu().numpy())
+    return got, int(step.err[0])
+
+
+@pytest.mark.parametrize("C,D,quant", [(6, 3, None), (100, 16, None), (700, 64, 16),
+                                       (2048, 64, None), (2048, 40, 4), (37, 37, None)])
+def test_tree_build_conditioned_random_forests(C, D, quant):
+    B = 4
+    w = W.WORKLOADS["qwen"].scaled(B=B, V=50000, P=64, P_min=64)
+    cp, ct, cpar = _random_forest(B, C, seed=C + D, quant=quant)
+    root = torch.arange(B, dtype=torch.int32)
+    ref = oracle.tree_conditioned(cp, ct, cpar, D, root.numpy())
+    assert (ref["status"] == 0).all()
+    got, err = run_conditioned(w, cp, ct, cpar, root, D)
+    assert err == 0
+    assert_tree_equal(got, ref)
+
+
+def test_tree_build_conditioned_page_toy_and_marginal_equivalence():
+    w = W.WORKLOADS["toy"]
+    cp = np.array([[0.5, 0.375, 0.625, 0.25, 0.5, 0.25]], np.float32)
+    ct = np.array([[1, 2, 1, 2, 0, 1]], np.int32)
+    cpar = np.array([[-1, -1, 0, 0, 1, 1]], np.int32)
+    root = torch.tensor([0], dtype=torch.int32)
+    got, err = run_conditioned(w.scaled(B=1), cp, ct, cpar, root, 3)
+    assert err == 0
+    assert got["token"][0].tolist() == [0, 1, 2, 1] and got["parent"][0].tolist() == [-1, 0, 0, 1]
+    # the full expansion of the qwen marginals equals tsd_tree_build's tree
+    d = inputs("qwen", S=3, k=8, D=40, V=3000)
+    wq = d["w"]
+    S, k = wq.S, wq.k
+    p, tok, par = [], [], []
+    level = [-1]
+    for s in range(S):
+        nxt = []
+        for pi in level:
+            for r in range(k):
+                p.append(d["tp"][0, s, r]); tok.append(d["ti"][0, s, r]); par.append(pi)
+                nxt.append(len(p) - 1)
+        level = nxt
+    got, err = run_conditioned(wq, np.array([p], np.float32), np.array([tok], np.int32),
+                               np.array([par], np.int32), d["root"], wq.D)
+    assert err == 0
+    assert_tree_equal(got, d["tree"])
+
+
+def test_tree_build_conditioned_reports_malformed_forest():
+    w = W.WORKLOADS["qwen"].scaled(B=2, V=50000, P=64, P_min=64)
+    cp, ct, cpar = _random_forest(2, 50, seed=1)
+    cpar[1, 10] = 20          # parent listed after its child: request 1 rejected
+    root = torch.tensor([5, 6], dtype=torch.int32)
+    got, err = run_conditioned(w, cp, ct, cpar, root, 8)
+    assert err == (T.TSD_DEV_ERR_BAD_TREE | 1)
+    assert got["token"][1].tolist() == [6] + [-1] * 8
+    ref = oracle.tree_conditioned(cp[:1], ct[:1], cpar[:1], 8, root.numpy()[:1])
+    assert got["token"][0].tolist() == ref["token"][0].tolist()

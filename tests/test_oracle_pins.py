@@ -481,3 +481,92 @@ def test_adaptive_extremes():
     assert oracle.adaptive_count(s, 1.0, np.array([0, 1e9, 1e9, 1e9, 1e9], np.float32)) == 0
     # zero-probability nodes never raise the objective
     assert oracle.adaptive_count(np.zeros(4, np.float32), 1.0, np.arange(5, dtype=np.float32)) == 0
+
+
+# ------------------------------------------- parent-conditioned proposals --
+# "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4" (review),
+# "How it works" steps 1-2: A expands B and C; B proposes B and C, C proposes
+# A and B; with D = 3 the kept nodes are A-B, A-C and A-B-B.
+
+TOY_FOREST = dict(
+    # candidates, parents first: B, C | B, C (children of B) | A, B (children of C)
+    p=[[0.5, 0.375, 0.625, 0.25, 0.5, 0.25]],
+    tok=[[1, 2, 1, 2, 0, 1]],
+    parent=[[-1, -1, 0, 0, 1, 1]],
+)
+
+
+def test_conditioned_toy_matches_page_example():
+    t = oracle.tree_conditioned(TOY_FOREST["p"], TOY_FOREST["tok"], TOY_FOREST["parent"], 3,
+                                np.array([0], np.int32))
+    # rows: A (root), A-B (0.5), A-C (0.375), A-B-B (0.3125); A-C-A (0.1875) is cut
+    assert t["token"][0].tolist() == [0, 1, 2, 1]
+    assert t["parent"][0].tolist() == [-1, 0, 0, 1]
+    assert t["score"][0].tolist() == [1.0, 0.5, 0.375, 0.3125]
+    assert t["mask"][0].tolist() == [0, 1, 2, 5]
+    assert t["is_leaf"][0].tolist() == [0, 0, 1, 1]
+    assert t["status"].tolist() == [0]
+
+
+def _bfs_forest(tp, ti):
+    """The full k-ary expansion of per-position marginals as a forest in BFS
+    order (children in rank order), B = 1."""
+    S, k = tp.shape
+    p, tok, par = [], [], []
+    level = [-1]
+    for s in range(S):
+        nxt = []
+        for parent_idx in level:
+            for r in range(k):
+                p.append(tp[s, r]); tok.append(ti[s, r]); par.append(parent_idx)
+                nxt.append(len(p) - 1)
+        level = nxt
+    return (np.array([p], np.float32), np.array([tok], np.int32), np.array([par], np.int32))
+
+
+@pytest.mark.parametrize("S,k,D,quant", [(2, 2, 3, None), (3, 3, 12, None), (3, 4, 20, 8),
+                                         (4, 2, 15, 4), (2, 5, 25, None)])
+def test_conditioned_on_marginal_expansion_equals_marginal_tree(S, k, D, quant):
+    """Proposals that ignore the parent (every node's children are the same
+    per-position top-k) give exactly the per-position tree, ties included:
+    BFS order with children in rank order is the rank-tuple order."""
+    rng = np.random.default_rng(S * 100 + k * 10 + D)
+    x = rng.normal(size=(1, S, 30)) * 2.0
+    pr = np.exp(x) / np.exp(x).sum(-1, keepdims=True)
+    if quant:
+        pr = np.round(pr * quant) / quant
+    tp, ti = oracle.topk(pr.astype(np.float32), k)
+    ref = oracle.tree(tp, ti, D, np.array([7], np.int32), method="enum")
+    cp, ct, cpar = _bfs_forest(tp[0], ti[0])
+    got = oracle.tree_conditioned(cp, ct, cpar, D, np.array([7], np.int32))
+    for key in ("token", "parent", "depth", "score", "mask", "is_leaf"):
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+
+
+def test_conditioned_tree_maximises_expected_acceptance():
+    """Method 2: among all ancestor-closed sets of D candidates, the kept set
+    has the largest sum of scores (brute force over small random forests)."""
+    rng = np.random.default_rng(5)
+    for _ in range(30):
+        C = int(rng.integers(5, 11))
+        par = [-1] + [int(rng.integers(-1, c)) for c in range(1, C)]
+        p = rng.uniform(0.05, 1.0, C).astype(np.float32)
+        D = int(rng.integers(1, min(C, 5) + 1))
+        t = oracle.tree_conditioned(p[None], np.arange(C, dtype=np.int32)[None],
+                                    np.array([par], np.int32), D, np.array([99], np.int32))
+        sc = np.zeros(C)
+        for c in range(C):
+            sc[c] = p[c] * (1.0 if par[c] < 0 else sc[par[c]])
+        best = 0.0
+        for sub in itertools.combinations(range(C), D):
+            ss = set(sub)
+            if all(par[c] < 0 or par[c] in ss for c in sub):
+                best = max(best, sum(sc[c] for c in sub))
+        assert abs(float(np.sum(t["score"][0, 1:], dtype=np.float64)) - best) < 1e-5
+
+
+def test_conditioned_rejects_malformed_forest():
+    t = oracle.tree_conditioned([[0.5, 0.5]], [[1, 2]], [[-1, 1]], 2, np.array([0], np.int32))
+    assert t["status"].tolist() == [1] and t["token"][0].tolist() == [0, -1, -1]
+    t = oracle.tree_conditioned([[0.5, 1.5]], [[1, 2]], [[-1, 0]], 2, np.array([0], np.int32))
+    assert t["status"].tolist() == [1]

@@ -42,7 +42,8 @@ TSD_BF16 = 1
 
 # every symbol the header declares
 EXPORTED = ("tsd_status_string", "tsd_version", "tsd_tree_build_workspace_size",
-            "tsd_tree_build", "tsd_tree_build_adaptive", "tsd_verify_workspace_size",
+            "tsd_tree_build", "tsd_tree_build_adaptive", "tsd_tree_build_conditioned",
+            "tsd_verify_workspace_size",
             "tsd_tree_verify_attn",
             "tsd_accept_walk_workspace_size", "tsd_accept_walk", "tsd_accept_walk_static",
             "tsd_commit_path")
@@ -76,6 +77,8 @@ def _load():
     lib.tsd_tree_build_adaptive.argtypes = [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, Z,
                                             P, P]
     lib.tsd_tree_build_adaptive.restype = I
+    lib.tsd_tree_build_conditioned.argtypes = [P, P, P, I, I, I, P, P, P, P, P, P, P, P, P]
+    lib.tsd_tree_build_conditioned.restype = I
     lib.tsd_verify_workspace_size.argtypes = [ctypes.POINTER(tsd_attn_desc)]
     lib.tsd_verify_workspace_size.restype = Z
     lib.tsd_tree_verify_attn.argtypes = [ctypes.POINTER(tsd_attn_desc), P, P, P, P, P, P, P, P,
@@ -161,6 +164,15 @@ def tsd_tree_build_adaptive(probs, k, D_max, root_tok, cost_d, cost_v, token, pa
         _ptr(probs), B, S, V, k, D_max, _ptr(root_tok), _ptr(cost_d), _ptr(cost_v), _ptr(token),
         _ptr(parent), _ptr(depth), _ptr(score), _ptr(mask), _ptr(is_leaf), _ptr(n_nodes),
         _ptr(ws), _nbytes(ws), _ptr(err), _stream(stream)))
+
+
+def tsd_tree_build_conditioned(cand_p, cand_tok, cand_parent, D, root_tok, token, parent, depth,
+                               score, mask, is_leaf, err=None, stream=None):
+    B, C = cand_p.shape
+    _check("tsd_tree_build_conditioned", lib.tsd_tree_build_conditioned(
+        _ptr(cand_p), _ptr(cand_tok), _ptr(cand_parent), B, C, D, _ptr(root_tok), _ptr(token),
+        _ptr(parent), _ptr(depth), _ptr(score), _ptr(mask), _ptr(is_leaf), _ptr(err),
+        _stream(stream)))
 
 
 def tsd_verify_workspace_size(desc: tsd_attn_desc) -> int:

@@ -22,7 +22,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtsd.so")
 
 SOURCES = ["tsd_api.cu", "tsd_tree_build.cu", "tsd_verify.cu", "tsd_verify_mma.cu",
-           "tsd_verify_tc.cu", "tsd_verify_mla.cu", "tsd_accept.cu", "tsd_commit.cu"]
+           "tsd_verify_tc.cu", "tsd_verify_mla.cu", "tsd_tree_cond.cu", "tsd_accept.cu",
+           "tsd_commit.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

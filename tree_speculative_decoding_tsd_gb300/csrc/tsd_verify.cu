@@ -19,9 +19,9 @@
 // Paths:
 //   generic (this file): CUDA-core fp32 arithmetic, one warp per key, lanes
 //     split the head dim, warp-shuffle reductions for q.k; any dtype/dims.
-//     Used for fp32 inputs (never TF32) and for fewer than 64 packed rows (not
-//     a dense contraction).
-//   tc (tsd_verify_tc.cu): bf16 GQA heads, head dim 128, >= 64 packed rows:
+//     Used for fp32 inputs (never TF32) and for bf16 heads with too few packed
+//     rows for a tensor-core tile (fewer than 16 on the tcgen05 path).
+//   tc (tsd_verify_tc.cu): bf16 GQA heads, head dim 128, >= 16 packed rows:
 //     tcgen05 MMAs with TMEM accumulators, TMA-fed K/V ring (the default).
 //     Latent heads (bf16, dk 576 / dv 512, V = K[:, :512]) with >= 64 packed
 //     rows take the tcgen05 kernel of tsd_verify_mla.cu.
@@ -173,16 +173,17 @@ static int choose_path(const tsd_attn_desc& d, int M) {
   const bool gqa_bf16 = d.dtype == TSD_BF16 && !d.v_aliases_k && d.dk == d.dv;
   const bool mma_ok = gqa_bf16 && (d.dk == 64 || d.dk == 128);
   const bool mla_bf16 = d.dtype == TSD_BF16 && d.v_aliases_k && d.dk == 576 && d.dv == 512;
-  const bool tc_ok = (gqa_bf16 && d.dk == 128 || mla_bf16) && M >= kMmaMinRows &&
-                     tc_path_available();
+  // tcgen05 with the packed rows on the MMA N dimension works from N = 16 up
+  const bool tc_ok = ((gqa_bf16 && d.dk == 128 && M >= kTcMinRows) ||
+                      (mla_bf16 && M >= kMmaMinRows)) && tc_path_available();
   const char* force = getenv("TSD_VERIFY_PATH");
   if (force != nullptr) {
     if (strcmp(force, "generic") == 0) return kPathGeneric;
     if (strcmp(force, "mma") == 0 && mma_ok) return kPathMma;
     if (strcmp(force, "tc") == 0 && tc_ok) return kPathTc;
   }
-  if (M < kMmaMinRows) return kPathGeneric;  // not a dense contraction
   if (tc_ok) return kPathTc;
+  if (M < kMmaMinRows) return kPathGeneric;  // not a dense contraction
   if (mma_ok) return kPathMma;
   return kPathGeneric;
 }

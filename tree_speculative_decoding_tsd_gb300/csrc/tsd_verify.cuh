@@ -42,8 +42,12 @@ struct VerifyPlan {
   size_t ws_bytes;
 };
 
-// Fewer packed rows than this are not a dense contraction: CUDA cores.
+// Fewer packed rows than this are not a dense contraction for the legacy
+// mma.sync path: CUDA cores.
 constexpr int kMmaMinRows = 64;
+// The tcgen05 path puts the packed rows on the MMA N dimension (a multiple of
+// 16), so it takes any count from 16 rows up.
+constexpr int kTcMinRows = 16;
 
 VerifyPlan plan_verify(const tsd_attn_desc& d);
 bool launch_mma_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPlan& p,

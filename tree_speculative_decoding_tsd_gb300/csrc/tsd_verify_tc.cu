@@ -1,5 +1,5 @@
 // tcgen05 (5th-generation tensor core) path of tsd_tree_verify_attn for bf16
-// GQA heads with dk == dv == 128 and at least 64 packed query rows.
+// GQA heads with dk == dv == 128 and at least 16 packed query rows.
 //
 // Layout choice.  The packed query rows of one KV head (R tree rows x g query
 // heads: 68, 132 or 260 for the workloads here) rarely fill 128-row MMA tiles,
@@ -587,6 +587,9 @@ bool launch_tc_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPla
       !encode_3d(&maps.vt, a.vt, d.Hkv, (long)d.B * d.R))
     return false;
   switch (p.rb) {
+    case 16: launch_tc<16>(maps, a, p, st); break;
+    case 32: launch_tc<32>(maps, a, p, st); break;
+    case 48: launch_tc<48>(maps, a, p, st); break;
     case 64: launch_tc<64>(maps, a, p, st); break;
     case 80: launch_tc<80>(maps, a, p, st); break;
     case 96: launch_tc<96>(maps, a, p, st); break;

@@ -13,8 +13,9 @@ import dataclasses
 import torch
 
 from . import (make_desc, tsd_accept_walk, tsd_accept_walk_workspace_size, tsd_commit_path,
-               tsd_tree_build, tsd_tree_build_adaptive, tsd_tree_build_workspace_size,
-               tsd_tree_verify_attn, tsd_verify_workspace_size, workspace)
+               tsd_tree_build, tsd_tree_build_adaptive, tsd_tree_build_conditioned,
+               tsd_tree_build_workspace_size, tsd_tree_verify_attn, tsd_verify_workspace_size,
+               workspace)
 
 
 @dataclasses.dataclass
@@ -79,6 +80,13 @@ class TreeVerifyStep:
                                 t.depth, t.score, t.mask, t.is_leaf, self.n_nodes, self.ws_build,
                                 self.err, stream)
 
+    def build_conditioned(self, cand_p, cand_tok, cand_parent, root_tok, stream=None):
+        """Tree from parent-conditioned proposals (a candidate forest [B][C])."""
+        t = self.tree
+        tsd_tree_build_conditioned(cand_p, cand_tok, cand_parent, self.D, root_tok, t.token,
+                                   t.parent, t.depth, t.score, t.mask, t.is_leaf, self.err,
+                                   stream)
+
     def verify(self, q, kcache, vcache, prefix_len, ktree, vtree, stream=None):
         tsd_tree_verify_attn(self.desc, q, kcache, vcache, prefix_len, ktree, vtree,
                              self.tree.mask, self.out, self.lse, self.ws_verify, self.err, stream)
@@ -97,7 +105,43 @@ class TreeVerifyStep:
     def run(self, probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits,
             stream=None):
         """The whole step: build -> verify -> accept -> commit (asynchronous)."""
-        self.build(probs, root_tok, stream)
+        self._round(probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits, None,
+                    None, stream)
+
+    def capture(self, probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits,
+                cost_d=None, cost_v=None, stream=None):
+        """Record the whole step as one CUDA graph on the given tensors.
+
+        Every buffer of the step is preallocated and every shape is fixed, and
+        all per-round metadata (tree rows, masks, accepted path, prefix
+        lengths, and with cost tables the per-request node count) lives on the
+        device, so one replay runs a full round with no host work: refill the
+        captured input tensors in place, then call ``replay()`` on the
+        returned graph.  With ``cost_d``/``cost_v`` the tree is built by the
+        cost-aware rule (rows past each request's count are padding).
+        """
+        import torch
+
+        if stream is None:
+            stream = torch.cuda.Stream(device=probs.device)
+        # one eager warm-up: lazy set-up (function attributes, tensor-map
+        # encoder lookup) must not happen during capture
+        with torch.cuda.stream(stream):
+            self._round(probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits,
+                        cost_d, cost_v, stream)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            self._round(probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits,
+                        cost_d, cost_v, stream)
+        return graph
+
+    def _round(self, probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits,
+               cost_d, cost_v, stream):
+        if cost_v is None:
+            self.build(probs, root_tok, stream)
+        else:
+            self.build_adaptive(probs, root_tok, cost_d, cost_v, stream)
         self.verify(q, kcache, vcache, prefix_len, ktree, vtree, stream)
         self.accept(logits, stream)
         self.commit(ktree, vtree, kcache, vcache, prefix_len, stream)
