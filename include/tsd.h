@@ -72,6 +72,7 @@ typedef enum {
 #define TSD_DEV_ERR_CAPACITY 0x01000000 /* commit would pass the cache capacity */
 #define TSD_DEV_ERR_BAD_TREE 0x02000000 /* parent/row out of range, walk deeper than S */
 #define TSD_DEV_ERR_TIMEOUT  0x03000000 /* a bounded wait inside a kernel gave up */
+#define TSD_DEV_ERR_BAD_PAGE 0x04000000 /* page table entry outside the page pool */
 #define TSD_DEV_ERR_MASK     0x7f000000
 
 /* Element types of attention operands. */
@@ -228,6 +229,46 @@ tsd_status tsd_tree_verify_attn(const tsd_attn_desc* desc, const void* q,
                                 void* out, float* lse, void* ws,
                                 size_t ws_bytes, int32_t* err,
                                 tsd_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * Paged KV cache: tsd_tree_verify_attn_paged, tsd_commit_path_paged
+ *
+ * The same calls over a cache held in fixed-size pages (V4 review, "Secret
+ * weapon": the persistent cache and the scratch pad are separate, and only
+ * the accepted path is written back).  The caller owns the pages and the
+ * page table; these calls neither allocate nor move pages.
+ *
+ * kpool, vpool  [num_pages][Hkv][page_size][dk | dv]: page pools, element type
+ *               as desc->dtype (vpool unused and may be NULL when V aliases K);
+ *               one head's rows of a page are contiguous.
+ * page_table    [B][max_pages] int32: page_table[b][j] is the pool page that
+ *               holds positions j*page_size .. (j+1)*page_size - 1 of request b.
+ * page_size     a multiple of 128; desc->cap must equal max_pages * page_size.
+ * Position pos of request b, head h, is row
+ *   (page_table[b][pos / page_size] * Hkv + h) * page_size + pos % page_size
+ * of the pool.  Everything else (arguments, outputs, workspace sizes,
+ * tolerances) is as for tsd_tree_verify_attn / tsd_commit_path; results are
+ * identical to those calls on the gathered contiguous cache.  Only the pages
+ * of positions the call reads (verify: 0..P-1) or writes (commit: P..P+L) are
+ * looked up; such an entry outside [0, num_pages) is never dereferenced and
+ * sets TSD_DEV_ERR_BAD_PAGE | b (verify: the request's output is not valid;
+ * commit: the request is skipped).
+ * -------------------------------------------------------------------------- */
+tsd_status tsd_tree_verify_attn_paged(const tsd_attn_desc* desc, const void* q,
+                                      const void* kpool, const void* vpool,
+                                      const int32_t* page_table, int max_pages,
+                                      int page_size, int num_pages,
+                                      const int32_t* prefix_len, const void* ktree,
+                                      const void* vtree, const uint64_t* mask,
+                                      void* out, float* lse, void* ws, size_t ws_bytes,
+                                      int32_t* err, tsd_stream_t stream);
+
+tsd_status tsd_commit_path_paged(const tsd_attn_desc* desc, int S, const void* ktree,
+                                 const void* vtree, const int32_t* accept_rows,
+                                 const int32_t* accept_len, void* kpool, void* vpool,
+                                 const int32_t* page_table, int max_pages, int page_size,
+                                 int num_pages, int32_t* prefix_len, int32_t* err,
+                                 tsd_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * tsd_accept_walk

@@ -130,3 +130,20 @@ def test_workspace_sizes_are_deterministic_and_scale():
     b = T.tsd_accept_walk_workspace_size(32, 32, 151936)
     assert b >= 32 * 33 * 8
     assert T.tsd_tree_build_workspace_size(0, 7, 100, 8) == 0
+
+
+@pytest.mark.parametrize("args", [dict(page_size=64), dict(page_size=100), dict(max_pages=3),
+                                  dict(table=N), dict(table=U), dict(num_pages=0)])
+def test_paged_calls_reject(args):
+    kw = dict(page_size=128, max_pages=4, num_pages=8, table=A)
+    kw.update(args)
+    d = _desc(cap=512)
+    st = T.lib.tsd_tree_verify_attn_paged(ctypes.byref(d), A, A, A, kw["table"], kw["max_pages"],
+                                          kw["page_size"], kw["num_pages"], A, A, A, A, A, A, A,
+                                          1 << 30, N, N)
+    assert st == T.TSD_ERR_INVALID_ARG
+    # every case here also fails the commit's checks (capacity != max_pages *
+    # page_size, or a bad table pointer, or no pages), so nothing is launched
+    st = T.lib.tsd_commit_path_paged(ctypes.byref(d), 3, A, A, A, A, A, A, kw["table"],
+                                     kw["max_pages"], kw["page_size"], kw["num_pages"], A, N, N)
+    assert st == T.TSD_ERR_INVALID_ARG

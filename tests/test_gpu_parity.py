@@ -783,3 +783,127 @@ def test_tree_build_conditioned_reports_malformed_forest():
     assert got["token"][1].tolist() == [6] + [-1] * 8
     ref = oracle.tree_conditioned(cp[:1], ct[:1], cpar[:1], 8, root.numpy()[:1])
     assert got["token"][0].tolist() == ref["token"][0].tolist()
+
+
+# --------------------------------------------------------- paged KV cache --
+
+def _paged(cache, page_size, seed, spare=3):
+    """Scatter a contiguous cache [B][Hkv][cap][d] (cap a multiple of
+    page_size) into a shuffled page pool [num_pages][Hkv][page_size][d]."""
+    B, Hkv, cap, dd = cache.shape
+    mp = cap // page_size
+    num_pages = B * mp + spare
+    perm = np.random.default_rng(seed).permutation(num_pages)[:B * mp].reshape(B, mp)
+    pool = torch.zeros((num_pages, Hkv, page_size, dd), dtype=cache.dtype)
+    for b in range(B):
+        for j in range(mp):
+            pool[perm[b, j]] = cache[b, :, j * page_size:(j + 1) * page_size]
+    return pool, torch.from_numpy(perm.astype(np.int32))
+
+
+def _gather(pool, table, page_size):
+    B, mp = table.shape
+    return torch.cat([torch.stack([pool[int(table[b, j])] for j in range(mp)], 1)
+                      .reshape(pool.shape[1], mp * page_size, pool.shape[3])[None]
+                      for b in range(B)])
+
+
+@pytest.mark.parametrize("name,over,page_size,force", [
+    ("qwen", dict(B=3, P=900, P_min=100, V=2000), 128, "tc"),
+    ("qwen", dict(B=3, P=900, P_min=100, V=2000), 256, "generic"),
+    ("mla", dict(B=2, P=700, P_min=300, V=2000), 128, "tc"),
+    ("toy", dict(), 128, None),
+])
+def test_paged_verify_equals_contiguous(name, over, page_size, force, monkeypatch):
+    """Verify through a shuffled page pool gives the same bytes as the
+    contiguous cache, and matches the oracle on the gathered cache."""
+    if force:
+        monkeypatch.setenv("TSD_VERIFY_PATH", force)
+    d = inputs(name, **over)
+    w = d["w"]
+    cap = -(-w.cap // page_size) * page_size
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    pad = cap - kc.shape[2]
+    kc = torch.nn.functional.pad(kc, (0, 0, 0, pad))
+    vc = None if vc is None else torch.nn.functional.pad(vc, (0, 0, 0, pad))
+    step = TreeVerifyStep(w.B, w.S, w.V, w.k, w.D, w.Hq, w.Hkv, w.dk, w.dv, cap, w.torch_dtype,
+                          w.v_aliases_k, w.scale, DEV)
+    step.tree.mask.copy_(torch.from_numpy(np.ascontiguousarray(d["tree"]["mask"]).view(np.int64)))
+    step.verify(*gpu(q, kc, vc, plen, kt, vt))
+    torch.cuda.synchronize()
+    out_c, lse_c = step.out.clone(), step.lse.clone()
+    kpool, table = _paged(kc, page_size, seed=7)
+    vpool = None if vc is None else _paged(vc, page_size, seed=7)[0]
+    g = gpu(q, kpool, vpool, table, plen, kt, vt)
+    T.tsd_tree_verify_attn_paged(step.desc, g[0], g[1], g[2], g[3], page_size, g[4], g[5], g[6],
+                                 step.tree.mask, step.out, step.lse, step.ws_verify, step.err)
+    torch.cuda.synchronize()
+    assert int(step.err[0]) == 0
+    assert torch.equal(step.out, out_c) and torch.equal(step.lse, lse_c)
+    kg = _gather(kpool, table, page_size)
+    assert torch.equal(kg, kc)
+    ref_out, _ = oracle.verify_attn(W.bits(q), W.bits(kg), None if vc is None else W.bits(vc),
+                                    plen.numpy(), W.bits(kt), None if vt is None else W.bits(vt),
+                                    d["tree"]["mask"], w.scale, v_aliases_k=w.v_aliases_k, dv=w.dv)
+    assert np.abs(step.out.float().cpu().numpy() - ref_out).max() <= _tol(w)
+
+
+@pytest.mark.parametrize("name", ["qwen", "mla"])
+def test_paged_commit_equals_contiguous(name):
+    d = inputs(name, B=3, P=500, P_min=100, V=2000)
+    w, tree = d["w"], d["tree"]
+    page_size = 128
+    cap = -(-w.cap // page_size) * page_size
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    pad = cap - kc.shape[2]
+    kc = torch.nn.functional.pad(kc, (0, 0, 0, pad))
+    vc = None if vc is None else torch.nn.functional.pad(vc, (0, 0, 0, pad))
+    step = TreeVerifyStep(w.B, w.S, w.V, w.k, w.D, w.Hq, w.Hkv, w.dk, w.dv, cap, w.torch_dtype,
+                          w.v_aliases_k, w.scale, DEV)
+    set_tree(step, tree)
+    tl = W.target_logits(w, torch.from_numpy(tree["depth"]), d["logits"])
+    step.accept(tl.to(DEV))
+    kpool, table = _paged(kc, page_size, seed=3)
+    vpool = None if vc is None else _paged(vc, page_size, seed=3)[0]
+    gc = gpu(kt, vt, kc, vc, plen)
+    step.commit(*gc)
+    gp = gpu(kt, vt, kpool, vpool, table, plen)
+    wk = step.walk
+    T.tsd_commit_path_paged(step.desc, w.S, gp[0], gp[1], wk.accept_rows, wk.accept_len, gp[2],
+                            gp[3], gp[4], page_size, gp[5], step.err)
+    torch.cuda.synchronize()
+    assert int(step.err[0]) == 0
+    assert torch.equal(gc[4], gp[5])
+    assert torch.equal(_gather(gp[2].cpu(), table, page_size), gc[2].cpu())
+    if vc is not None:
+        assert torch.equal(_gather(gp[3].cpu(), table, page_size), gc[3].cpu())
+
+
+def test_paged_bad_page_is_reported_not_read():
+    d = inputs("qwen", B=2, P=600, P_min=600, V=2000)
+    w = d["w"]
+    page_size = 128
+    cap = -(-w.cap // page_size) * page_size
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    kc = torch.nn.functional.pad(kc, (0, 0, 0, cap - kc.shape[2]))
+    vc = torch.nn.functional.pad(vc, (0, 0, 0, cap - vc.shape[2]))
+    kpool, table = _paged(kc, page_size, seed=1)
+    vpool = _paged(vc, page_size, seed=1)[0]
+    table[1, 2] = kpool.shape[0] + 100     # request 1, positions 256..383: outside the pool
+    import os
+    for force in ("tc", "generic"):
+        os.environ["TSD_VERIFY_PATH"] = force
+        try:
+            # the workspace follows the plan of the forced path
+            step = TreeVerifyStep(w.B, w.S, w.V, w.k, w.D, w.Hq, w.Hkv, w.dk, w.dv, cap,
+                                  w.torch_dtype, w.v_aliases_k, w.scale, DEV)
+            step.tree.mask.copy_(
+                torch.from_numpy(np.ascontiguousarray(d["tree"]["mask"]).view(np.int64)))
+            g = gpu(q, kpool, vpool, table, plen, kt, vt)
+            T.tsd_tree_verify_attn_paged(step.desc, g[0], g[1], g[2], g[3], page_size, g[4], g[5],
+                                         g[6], step.tree.mask, step.out, step.lse, step.ws_verify,
+                                         step.err)
+            torch.cuda.synchronize()
+        finally:
+            os.environ.pop("TSD_VERIFY_PATH", None)
+        assert int(step.err[0]) == (T.TSD_DEV_ERR_BAD_PAGE | 1), force

@@ -35,6 +35,7 @@ TSD_ERR_DEVICE = 4
 TSD_ERR_DEVICE_TIMEOUT = 5
 TSD_DEV_ERR_CAPACITY = 0x01000000
 TSD_DEV_ERR_BAD_TREE = 0x02000000
+TSD_DEV_ERR_BAD_PAGE = 0x04000000
 TSD_DEV_ERR_TIMEOUT = 0x03000000
 TSD_DEV_ERR_MASK = 0x7F000000
 TSD_F32 = 0
@@ -44,7 +45,7 @@ TSD_BF16 = 1
 EXPORTED = ("tsd_status_string", "tsd_version", "tsd_tree_build_workspace_size",
             "tsd_tree_build", "tsd_tree_build_adaptive", "tsd_tree_build_conditioned",
             "tsd_verify_workspace_size",
-            "tsd_tree_verify_attn",
+            "tsd_tree_verify_attn", "tsd_tree_verify_attn_paged", "tsd_commit_path_paged",
             "tsd_accept_walk_workspace_size", "tsd_accept_walk", "tsd_accept_walk_static",
             "tsd_commit_path")
 
@@ -92,6 +93,12 @@ def _load():
     lib.tsd_accept_walk_static.restype = I
     lib.tsd_commit_path.argtypes = [ctypes.POINTER(tsd_attn_desc), I, P, P, P, P, P, P, P, P, P]
     lib.tsd_commit_path.restype = I
+    lib.tsd_tree_verify_attn_paged.argtypes = [ctypes.POINTER(tsd_attn_desc), P, P, P, P, I, I, I,
+                                               P, P, P, P, P, P, P, Z, P, P]
+    lib.tsd_tree_verify_attn_paged.restype = I
+    lib.tsd_commit_path_paged.argtypes = [ctypes.POINTER(tsd_attn_desc), I, P, P, P, P, P, P, P, I,
+                                          I, I, P, P, P]
+    lib.tsd_commit_path_paged.restype = I
     return lib
 
 
@@ -208,6 +215,24 @@ def tsd_accept_walk_static(logits, S, token, parent, mask, is_leaf, tgt, accept_
         _ptr(logits), B, R - 1, S, V, _ptr(token), _ptr(parent), _ptr(mask), _ptr(is_leaf),
         _ptr(tgt), _ptr(accept_len), _ptr(accept_rows), _ptr(bonus), _ptr(chain_id), _ptr(err),
         _stream(stream)))
+
+
+def tsd_tree_verify_attn_paged(desc, q, kpool, vpool, page_table, page_size, prefix_len, ktree,
+                               vtree, mask, out, lse, ws, err=None, stream=None):
+    """page_table [B][max_pages] int32; pools [num_pages][Hkv][page_size][d]."""
+    _check("tsd_tree_verify_attn_paged", lib.tsd_tree_verify_attn_paged(
+        ctypes.byref(desc), _ptr(q), _ptr(kpool), _ptr(vpool), _ptr(page_table),
+        page_table.shape[1], page_size, kpool.shape[0], _ptr(prefix_len), _ptr(ktree),
+        _ptr(vtree), _ptr(mask), _ptr(out), _ptr(lse), _ptr(ws), _nbytes(ws), _ptr(err),
+        _stream(stream)))
+
+
+def tsd_commit_path_paged(desc, S, ktree, vtree, accept_rows, accept_len, kpool, vpool,
+                          page_table, page_size, prefix_len, err=None, stream=None):
+    _check("tsd_commit_path_paged", lib.tsd_commit_path_paged(
+        ctypes.byref(desc), S, _ptr(ktree), _ptr(vtree), _ptr(accept_rows), _ptr(accept_len),
+        _ptr(kpool), _ptr(vpool), _ptr(page_table), page_table.shape[1], page_size,
+        kpool.shape[0], _ptr(prefix_len), _ptr(err), _stream(stream)))
 
 
 def tsd_commit_path(desc, S, ktree, vtree, accept_rows, accept_len, kcache, vcache, prefix_len,

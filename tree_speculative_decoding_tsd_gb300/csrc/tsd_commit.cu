@@ -37,7 +37,19 @@ struct CommitArgs {
   int R, Hkv, cap, S;
   int kvec, vvec;   // 16-byte vectors per K row / V row (vvec = 0 if V aliases K)
   long krow, vrow;  // bytes per K row / V row
+  // paged cache (page_size > 0): position pos of request b lives in page
+  // page_table[b][pos / page_size] of the pools [num_pages][Hkv][page_size][row]
+  const int32_t* page_table;
+  int max_pages, page_size, num_pages;
 };
+
+// Cache row of position pos of (request b, head h); -1 for a page outside the pool.
+__device__ __forceinline__ long cache_row(const CommitArgs& a, int b, int h, int pos) {
+  if (a.page_size == 0) return ((long)b * a.Hkv + h) * a.cap + pos;
+  const int pg = a.page_table[(long)b * a.max_pages + pos / a.page_size];
+  if (pg < 0 || pg >= a.num_pages) return -1;
+  return ((long)pg * a.Hkv + h) * a.page_size + pos % a.page_size;
+}
 
 __global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kCommitThreads)
 commit_path_kernel(CommitArgs a) {
@@ -52,8 +64,10 @@ commit_path_kernel(CommitArgs a) {
   if (L < 0 || L > a.S) code = TSD_DEV_ERR_BAD_TREE;
   else if (P < 0 || (long)P + 1 + L > a.cap) code = TSD_DEV_ERR_CAPACITY;
   else
-    for (int i = 0; i <= L; ++i)
+    for (int i = 0; i <= L; ++i) {
       if (rows[i] < 0 || rows[i] >= a.R) code = TSD_DEV_ERR_BAD_TREE;
+      else if (cache_row(a, b, 0, P + i) < 0) code = TSD_DEV_ERR_BAD_PAGE;
+    }
 
   if (code == 0) {
     const int per_head = a.kvec + a.vvec;
@@ -65,7 +79,7 @@ commit_path_kernel(CommitArgs a) {
       const int h = rem / per_head;
       const int e = rem - h * per_head;
       const long src_row = ((long)b * a.R + rows[i]) * a.Hkv + h;
-      const long dst_row = ((long)b * a.Hkv + h) * a.cap + (P + i);
+      const long dst_row = cache_row(a, b, h, P + i);
       const int4* src;
       int4* dst;
       if (e < a.kvec) {
@@ -91,10 +105,11 @@ commit_path_kernel(CommitArgs a) {
 
 using namespace tsd;
 
-extern "C" tsd_status tsd_commit_path(const tsd_attn_desc* d, int S, const void* ktree,
-                                      const void* vtree, const int32_t* accept_rows,
-                                      const int32_t* accept_len, void* kcache, void* vcache,
-                                      int32_t* prefix_len, int32_t* err, tsd_stream_t stream) {
+static tsd_status commit_impl(const tsd_attn_desc* d, int S, const void* ktree, const void* vtree,
+                              const int32_t* accept_rows, const int32_t* accept_len, void* kcache,
+                              void* vcache, const int32_t* page_table, int max_pages,
+                              int page_size, int num_pages, int32_t* prefix_len, int32_t* err,
+                              tsd_stream_t stream) {
   if (d == nullptr) return TSD_ERR_INVALID_ARG;
   if (d->B < 1 || d->B > 65535 || d->R < 1 || d->R > 65 || d->Hkv < 1 || d->dk < 1 ||
       d->cap < 1 || S < 1 || S > 16)
@@ -109,6 +124,10 @@ extern "C" tsd_status tsd_commit_path(const tsd_attn_desc* d, int S, const void*
       !ok_ptr(prefix_len) || (((uintptr_t)err) & 3u) != 0)
     return TSD_ERR_INVALID_ARG;
   if (!alias && (!ok_ptr(vtree) || !ok_ptr(vcache))) return TSD_ERR_INVALID_ARG;
+  const bool paged = page_size > 0;
+  if (paged && (max_pages < 1 || num_pages < 1 || (long)max_pages * page_size != d->cap ||
+                !ok_ptr(page_table)))
+    return TSD_ERR_INVALID_ARG;
 
   CommitArgs a;
   a.ktree = (const char*)ktree;
@@ -127,7 +146,30 @@ extern "C" tsd_status tsd_commit_path(const tsd_attn_desc* d, int S, const void*
   a.vrow = alias ? 0 : (long)d->dv * es;
   a.kvec = (int)(a.krow / 16);
   a.vvec = (int)(a.vrow / 16);
+  a.page_table = paged ? page_table : nullptr;
+  a.max_pages = paged ? max_pages : 0;
+  a.page_size = paged ? page_size : 0;
+  a.num_pages = paged ? num_pages : 0;
   const dim3 grid(kCommitCluster, d->B);
   commit_path_kernel<<<grid, kCommitThreads, 0, (cudaStream_t)stream>>>(a);
   return cuda_status();
+}
+
+extern "C" tsd_status tsd_commit_path(const tsd_attn_desc* d, int S, const void* ktree,
+                                      const void* vtree, const int32_t* accept_rows,
+                                      const int32_t* accept_len, void* kcache, void* vcache,
+                                      int32_t* prefix_len, int32_t* err, tsd_stream_t stream) {
+  return commit_impl(d, S, ktree, vtree, accept_rows, accept_len, kcache, vcache, nullptr, 0, 0,
+                     0, prefix_len, err, stream);
+}
+
+extern "C" tsd_status tsd_commit_path_paged(const tsd_attn_desc* d, int S, const void* ktree,
+                                            const void* vtree, const int32_t* accept_rows,
+                                            const int32_t* accept_len, void* kpool, void* vpool,
+                                            const int32_t* page_table, int max_pages,
+                                            int page_size, int num_pages, int32_t* prefix_len,
+                                            int32_t* err, tsd_stream_t stream) {
+  if (page_size < 1) return TSD_ERR_INVALID_ARG;
+  return commit_impl(d, S, ktree, vtree, accept_rows, accept_len, kpool, vpool, page_table,
+                     max_pages, page_size, num_pages, prefix_len, err, stream);
 }

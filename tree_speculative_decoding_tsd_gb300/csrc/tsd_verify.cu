@@ -114,12 +114,16 @@ verify_generic_kernel(VerifyArgs a) {
     }
   };
 
-  const long head = (long)b * a.Hkv + hk;
-  const T* kbase = (const T*)a.kc + head * a.cap * DK;
-  const T* vbase = ALIAS ? kbase : (const T*)a.vc + head * a.cap * DV;
   constexpr int vstride = ALIAS ? DK : DV;
-  for (int j = k0 + warp; j < k1; j += kGenWarps)
-    visit(kbase + (long)j * DK, vbase + (long)j * vstride, false, j);
+  for (int j = k0 + warp; j < k1; j += kGenWarps) {
+    const long row = kv_row(a, b, hk, j);
+    if (row < 0) {   // page outside the pool: reported, never read
+      if (lane == 0) report_error(a.err, TSD_DEV_ERR_BAD_PAGE, b);
+      continue;
+    }
+    const T* kr = (const T*)a.kc + row * DK;
+    visit(kr, ALIAS ? kr : (const T*)a.vc + row * DV, false, j);
+  }
   if (with_tree) {
     const T* kt = (const T*)a.kt + ((long)b * a.R * a.Hkv + hk) * DK;
     const T* vt = ALIAS ? kt : (const T*)a.vt + ((long)b * a.R * a.Hkv + hk) * DV;
@@ -297,19 +301,26 @@ extern "C" size_t tsd_verify_workspace_size(const tsd_attn_desc* d) {
   return plan_verify(*d).ws_bytes;
 }
 
-extern "C" tsd_status tsd_tree_verify_attn(const tsd_attn_desc* d, const void* q,
-                                           const void* kcache, const void* vcache,
-                                           const int32_t* prefix_len, const void* ktree,
-                                           const void* vtree, const uint64_t* mask, void* out,
-                                           float* lse, void* ws, size_t ws_bytes, int32_t* err,
-                                           tsd_stream_t stream) {
+static tsd_status verify_impl(const tsd_attn_desc* d, const void* q, const void* kcache,
+                              const void* vcache, const int32_t* page_table, int max_pages,
+                              int page_size, int num_pages, const int32_t* prefix_len,
+                              const void* ktree, const void* vtree, const uint64_t* mask,
+                              void* out, float* lse, void* ws, size_t ws_bytes, int32_t* err,
+                              tsd_stream_t stream) {
   if (!desc_ok(d)) return TSD_ERR_INVALID_ARG;
   if ((((uintptr_t)err) & 3u) != 0) return TSD_ERR_INVALID_ARG;
   if (!ok_ptr(q) || !ok_ptr(kcache) || !ok_ptr(prefix_len) || !ok_ptr(ktree) || !ok_ptr(mask) ||
       !ok_ptr(out) || !ok_ptr(lse))
     return TSD_ERR_INVALID_ARG;
   if (!d->v_aliases_k && (!ok_ptr(vcache) || !ok_ptr(vtree))) return TSD_ERR_INVALID_ARG;
-  const VerifyPlan p = plan_verify(*d);
+  const bool paged = page_size > 0;
+  if (paged && (page_size % 128 != 0 || max_pages < 1 || num_pages < 1 ||
+                (long)max_pages * page_size != d->cap || !ok_ptr(page_table) ||
+                (long)num_pages * d->Hkv * page_size > (1l << 31)))
+    return TSD_ERR_INVALID_ARG;
+  VerifyPlan p = plan_verify(*d);
+  // the legacy mma.sync kernel addresses a contiguous cache only
+  if (paged && p.path == kPathMma) p.path = kPathGeneric;
   if (ws_bytes < p.ws_bytes || (p.ws_bytes > 0 && !ok_ptr(ws))) return TSD_ERR_INVALID_ARG;
 
   VerifyArgs a{};
@@ -323,6 +334,10 @@ extern "C" tsd_status tsd_tree_verify_attn(const tsd_attn_desc* d, const void* q
   a.nsplit = p.nsplit; a.split_len = p.split_len; a.nrg = p.nrg;
   a.qscale = d->scale * 1.4426950408889634f;
   a.err = err;
+  a.page_table = paged ? page_table : nullptr;
+  a.max_pages = paged ? max_pages : 0;
+  a.page_size = paged ? page_size : 0;
+  a.num_pages = paged ? num_pages : 0;
   const cudaStream_t st = (cudaStream_t)stream;
   bool launched;
   if (p.path == kPathTc && d->v_aliases_k) launched = launch_mla_tc_path(*d, a, p, st);
@@ -331,4 +346,27 @@ extern "C" tsd_status tsd_tree_verify_attn(const tsd_attn_desc* d, const void* q
   else launched = launch_generic_path(*d, a, p, st);
   if (!launched) return TSD_ERR_UNSUPPORTED;
   return cuda_status();
+}
+
+extern "C" tsd_status tsd_tree_verify_attn(const tsd_attn_desc* d, const void* q,
+                                           const void* kcache, const void* vcache,
+                                           const int32_t* prefix_len, const void* ktree,
+                                           const void* vtree, const uint64_t* mask, void* out,
+                                           float* lse, void* ws, size_t ws_bytes, int32_t* err,
+                                           tsd_stream_t stream) {
+  return verify_impl(d, q, kcache, vcache, nullptr, 0, 0, 0, prefix_len, ktree, vtree, mask, out,
+                     lse, ws, ws_bytes, err, stream);
+}
+
+extern "C" tsd_status tsd_tree_verify_attn_paged(const tsd_attn_desc* d, const void* q,
+                                                 const void* kpool, const void* vpool,
+                                                 const int32_t* page_table, int max_pages,
+                                                 int page_size, int num_pages,
+                                                 const int32_t* prefix_len, const void* ktree,
+                                                 const void* vtree, const uint64_t* mask,
+                                                 void* out, float* lse, void* ws, size_t ws_bytes,
+                                                 int32_t* err, tsd_stream_t stream) {
+  if (page_size < 1) return TSD_ERR_INVALID_ARG;
+  return verify_impl(d, q, kpool, vpool, page_table, max_pages, page_size, num_pages, prefix_len,
+                     ktree, vtree, mask, out, lse, ws, ws_bytes, err, stream);
 }

@@ -29,6 +29,10 @@ struct VerifyArgs {
   int B, R, Hq, Hkv, g, M, cap;
   int nsplit, split_len, nrg;
   float qscale;   // softmax scale * log2(e): scores are kept in the log2 domain
+  // paged cache (page_size > 0): kc/vc are page pools [num_pages][Hkv][page_size][d]
+  // and key `pos` of request b lives in page page_table[b][pos / page_size]
+  const int32_t* page_table;
+  int max_pages, page_size, num_pages;
 };
 
 enum VerifyPathId { kPathGeneric = 0, kPathMma = 1, kPathTc = 2 };
@@ -59,6 +63,16 @@ bool launch_mla_tc_path(const tsd_attn_desc& d, const VerifyArgs& a, const Verif
 bool tc_path_available();
 
 namespace {
+
+// Row of key `pos` of (request b, KV head hk) in the cache, or in the page
+// pool for a paged cache; -1 for a page index outside the pool (the caller
+// reports TSD_DEV_ERR_BAD_PAGE and never dereferences it).
+__device__ __forceinline__ long kv_row(const VerifyArgs& a, int b, int hk, int pos) {
+  if (a.page_size == 0) return ((long)b * a.Hkv + hk) * a.cap + pos;
+  const int pg = a.page_table[(long)b * a.max_pages + pos / a.page_size];
+  if (pg < 0 || pg >= a.num_pages) return -1;
+  return ((long)pg * a.Hkv + hk) * a.page_size + pos % a.page_size;
+}
 
 template <typename T> __device__ __forceinline__ T cvt_out(float x);
 template <> __device__ __forceinline__ float cvt_out<float>(float x) { return x; }

@@ -162,7 +162,16 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_p
     return true;
   };
 
-  auto ycoord = [&](int t) { return (b * a.Hkv + hk) * a.cap + k0 + t * kKeys; };
+  // first row of prefix tile t (a tile never crosses a page: page sizes are
+  // multiples of 128); a page outside the pool reads row 0 and is reported
+  auto ycoord = [&](int t) {
+    const long row = kv_row(a, b, hk, k0 + t * kKeys);
+    if (row < 0) {
+      report_error(a.err, TSD_DEV_ERR_BAD_PAGE, b);
+      return 0;
+    }
+    return (int)row;
+  };
   // box of pieces z, z+1 of tile t
   auto load_box = [&](uint32_t dst, int t, int z, uint32_t fb) {
     if (t < n_pre) tma_3d(dst, &maps.k, 0, ycoord(t), z, fb);
@@ -637,7 +646,9 @@ bool launch_mla_tc_path(const tsd_attn_desc& d, const VerifyArgs& a, const Verif
   if (d.dk != kDK || d.dv != kDV || !d.v_aliases_k || d.dtype != TSD_BF16) return false;
   if (encode_fn() == nullptr || p.rb != 64) return false;
   MlaMaps maps;
-  if (!encode_latent(&maps.k, a.kc, (long)d.B * d.Hkv * d.cap) ||
+  const long cache_rows = a.page_size > 0 ? (long)a.num_pages * d.Hkv * a.page_size
+                                          : (long)d.B * d.Hkv * d.cap;
+  if (!encode_latent(&maps.k, a.kc, cache_rows) ||
       !encode_latent_tree(&maps.kt, a.kt, d.Hkv, (long)d.B * d.R))
     return false;
   launch_mla<64>(maps, a, p, st);

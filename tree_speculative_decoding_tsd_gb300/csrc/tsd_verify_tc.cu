@@ -126,7 +126,16 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
   // ---------------------------------------------------------------- set-up
   // The TMA thread initialises the barriers and starts the first loads at
   // once, so they overlap the Q staging and the TMEM allocation.
-  auto ycoord = [&](int t) { return (b * a.Hkv + hk) * a.cap + k0 + t * kKeys; };
+  // first row of prefix tile t (a tile never crosses a page: page sizes are
+  // multiples of 128); a page outside the pool reads row 0 and is reported
+  auto ycoord = [&](int t) {
+    const long row = kv_row(a, b, hk, k0 + t * kKeys);
+    if (row < 0) {
+      report_error(a.err, TSD_DEV_ERR_BAD_PAGE, b);
+      return 0;
+    }
+    return (int)row;
+  };
   auto tma_k = [&](int t, int stage) {
     const uint32_t dst = sbase + kOffK + stage * kTileBytes;
     const uint32_t fb = bar(BAR_K_FULL + stage);
@@ -581,8 +590,9 @@ bool launch_tc_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPla
   if (d.dk != kD || d.dv != kD || d.v_aliases_k || d.dtype != TSD_BF16) return false;
   if (encode_fn() == nullptr) return false;
   TcMaps maps;
-  if (!encode_2d(&maps.k, a.kc, (long)d.B * d.Hkv * d.cap) ||
-      !encode_2d(&maps.v, a.vc, (long)d.B * d.Hkv * d.cap) ||
+  const long cache_rows = a.page_size > 0 ? (long)a.num_pages * d.Hkv * a.page_size
+                                          : (long)d.B * d.Hkv * d.cap;
+  if (!encode_2d(&maps.k, a.kc, cache_rows) || !encode_2d(&maps.v, a.vc, cache_rows) ||
       !encode_3d(&maps.kt, a.kt, d.Hkv, (long)d.B * d.R) ||
       !encode_3d(&maps.vt, a.vt, d.Hkv, (long)d.B * d.R))
     return false;
