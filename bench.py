@@ -414,6 +414,8 @@ def run_ours(args, dist):
 
     # ---- cost-aware adaptive budget (tsd_tree_build_adaptive) ----
     adaptive = run_adaptive(args, w, step, d, dev, stream)
+    # ---- the same verify through a shuffled page pool ----
+    paged = run_paged(args, w, step, d, dev, stream, plen0)
 
     nodes = w.B * w.D
     value = nodes * dist.world / (ms / 1e3)
@@ -457,6 +459,7 @@ def run_ours(args, dist):
         "device_err_word": err_word,
         "mean_accept_len": float(step.walk.accept_len.float().mean().item()),
         "adaptive": adaptive,
+        "paged": paged,
     }
     if tensor_bound:
         tpeak, tkind = load_tensor_peak()
@@ -469,6 +472,49 @@ def run_ours(args, dist):
                             "algorithmic_flops_per_launch": fl, "traffic": traffic_val,
                             "algorithmic_bytes_per_launch": algo["verify"]}
     return line, w, host
+
+
+def run_paged(args, w, step, d, dev, stream, plen0, page_size=128):
+    """tsd_tree_verify_attn_paged on the workload's cache scattered over a
+    shuffled pool of 128-token pages (per-call CUDA events, eager), next to the
+    contiguous verify of the same step."""
+    import tree_speculative_decoding_tsd_gb300 as T
+    cap = -(-w.cap // page_size) * page_size
+    mp = cap // page_size
+    g = torch.Generator(device="cpu").manual_seed(1234)
+    perm = torch.randperm(w.B * mp, generator=g).to(dev)
+
+    def to_pool(c):
+        if c is None:
+            return None
+        c = torch.nn.functional.pad(c, (0, 0, 0, cap - c.shape[2]))
+        pages = c.view(w.B, w.Hkv, mp, page_size, c.shape[3]).permute(0, 2, 1, 3, 4)
+        pool = torch.empty((w.B * mp, w.Hkv, page_size, c.shape[3]), dtype=c.dtype, device=dev)
+        pool[perm] = pages.reshape(w.B * mp, w.Hkv, page_size, c.shape[3])
+        return pool
+
+    kpool, vpool = to_pool(d["kc"]), to_pool(d["vc"])
+    table = perm.view(w.B, mp).to(torch.int32).contiguous()
+    desc = T.make_desc(w.B, w.R, w.Hq, w.Hkv, w.dk, w.dv, cap, w.torch_dtype, w.v_aliases_k,
+                       w.scale)
+    ws = T.workspace(T.tsd_verify_workspace_size(desc), dev)
+    t = step.tree
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        d["plen"].copy_(plen0)
+        for i in range(3 + args.steps):
+            if i >= 3:
+                ev[i - 3][0].record(stream)
+            T.tsd_tree_verify_attn_paged(desc, d["q"], kpool, vpool, table, page_size, d["plen"],
+                                         d["kt"], d["vt"], t.mask, step.out, step.lse, ws,
+                                         step.err, stream)
+            if i >= 3:
+                ev[i - 3][1].record(stream)
+    torch.cuda.synchronize(dev)
+    us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    del kpool, vpool
+    return {"verify_us": round(us, 2), "page_size": page_size, "pages": w.B * mp}
 
 
 def run_adaptive(args, w, step, d, dev, stream):

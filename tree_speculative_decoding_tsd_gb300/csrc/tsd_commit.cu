@@ -8,21 +8,17 @@
 // the next round starts from the extended prefix.  (Token-level KV refresh is
 // all a sliding-window / dense cache needs.)
 //
-// K6 commit_path_kernel: one cluster of 8 CTAs per request.  The CTAs split
-// the (row, head, K|V, 16-byte vector) copies between them; every CTA reads
-// the old prefix length before the cluster barrier, and CTA 0 of the cluster
-// writes the new one after it, so no CTA can see a half-updated length.
-#include <cooperative_groups.h>
-
+// K6 commit_path_kernel: one CTA per request.  Its threads split the (row,
+// head, K|V, 16-byte vector) copies; every thread reads the old prefix length
+// before the block barrier and thread 0 writes the new one after it.  (At most
+// (S+1) x Hkv rows of a few KB move per request: one CTA is enough, and a
+// cluster's launch and barrier cost more than they save.)
 #include "tsd_common.cuh"
 #include "tsd_host.h"
-
-namespace cg = cooperative_groups;
 
 namespace tsd {
 namespace {
 
-constexpr int kCommitCluster = 8;
 constexpr int kCommitThreads = 256;
 
 struct CommitArgs {
@@ -51,11 +47,8 @@ __device__ __forceinline__ long cache_row(const CommitArgs& a, int b, int h, int
   return ((long)pg * a.Hkv + h) * a.page_size + pos % a.page_size;
 }
 
-__global__ void __cluster_dims__(kCommitCluster, 1, 1) __launch_bounds__(kCommitThreads)
-commit_path_kernel(CommitArgs a) {
-  cg::cluster_group cluster = cg::this_cluster();
-  const int b = blockIdx.y;
-  const int rank = blockIdx.x;  // == cluster rank: one cluster spans gridDim.x
+__global__ void __launch_bounds__(kCommitThreads) commit_path_kernel(CommitArgs a) {
+  const int b = blockIdx.x;
   const int P = a.prefix_len[b];
   const int L = a.accept_len[b];
   const int32_t* rows = a.accept_rows + (long)b * (a.S + 1);
@@ -72,8 +65,7 @@ commit_path_kernel(CommitArgs a) {
   if (code == 0) {
     const int per_head = a.kvec + a.vvec;
     const long work = (long)(L + 1) * a.Hkv * per_head;
-    for (long w = (long)rank * kCommitThreads + threadIdx.x; w < work;
-         w += (long)kCommitCluster * kCommitThreads) {
+    for (long w = threadIdx.x; w < work; w += kCommitThreads) {
       const int i = (int)(w / ((long)a.Hkv * per_head));
       const int rem = (int)(w - (long)i * a.Hkv * per_head);
       const int h = rem / per_head;
@@ -92,9 +84,9 @@ commit_path_kernel(CommitArgs a) {
       *dst = __ldg(src);
     }
   }
-  // every CTA has read prefix_len[b] before anyone passes this barrier
-  cluster.sync();
-  if (rank == 0 && threadIdx.x == 0) {
+  // every thread has read prefix_len[b] before anyone passes this barrier
+  __syncthreads();
+  if (threadIdx.x == 0) {
     if (code == 0) a.prefix_len[b] = P + 1 + L;
     else report_error(a.err, code, b);
   }
@@ -150,8 +142,7 @@ static tsd_status commit_impl(const tsd_attn_desc* d, int S, const void* ktree, 
   a.max_pages = paged ? max_pages : 0;
   a.page_size = paged ? page_size : 0;
   a.num_pages = paged ? num_pages : 0;
-  const dim3 grid(kCommitCluster, d->B);
-  commit_path_kernel<<<grid, kCommitThreads, 0, (cudaStream_t)stream>>>(a);
+  commit_path_kernel<<<d->B, kCommitThreads, 0, (cudaStream_t)stream>>>(a);
   return cuda_status();
 }
 

@@ -64,25 +64,29 @@ __device__ __forceinline__ bool precedes(float sa, int da, uint64_t a0, uint64_t
   return a1 < b1;
 }
 
-// Per-lane register slots: frontier entry / row e lives in lane e % 32, slot e / 32.
-constexpr int kSlots = (kMaxD + 2 + 31) / 32;
-template <typename T>
-__device__ __forceinline__ T pick(const T (&v)[kSlots], int j) {
+// Per-lane register slots: frontier entry / row e lives in lane e % 32, slot
+// e / 32.  The frontier never holds more than D + 1 entries and there are D + 1
+// rows, so ceil((D + 2) / 32) slots suffice; the kernel is instantiated for
+// 1, 2 and 3 slots (D <= 30, 62, 64) because every pick and put costs one
+// select per slot.
+template <int NS, typename T>
+__device__ __forceinline__ T pick(const T (&v)[NS], int j) {
   T r = v[0];
 #pragma unroll
-  for (int i = 1; i < kSlots; ++i) r = (j == i) ? v[i] : r;
+  for (int i = 1; i < NS; ++i) r = (j == i) ? v[i] : r;
   return r;
 }
-template <typename T>
-__device__ __forceinline__ void put(T (&v)[kSlots], int j, T x, bool pred) {
+template <int NS, typename T>
+__device__ __forceinline__ void put(T (&v)[NS], int j, T x, bool pred) {
 #pragma unroll
-  for (int i = 0; i < kSlots; ++i) v[i] = (pred && j == i) ? x : v[i];
+  for (int i = 0; i < NS; ++i) v[i] = (pred && j == i) ? x : v[i];
 }
-template <typename T>
-__device__ __forceinline__ T bcast(const T (&v)[kSlots], int e) {
-  return __shfl_sync(kFull, pick(v, e >> 5), e & 31);
+template <int NS, typename T>
+__device__ __forceinline__ T bcast(const T (&v)[NS], int e) {
+  return __shfl_sync(kFull, pick<NS>(v, e >> 5), e & 31);
 }
 
+template <int kSlots>
 __global__ void __launch_bounds__(32 * kMaxS)
 best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, int nchunk,
                        const int32_t* __restrict__ root_tok, int32_t* __restrict__ token,
@@ -195,7 +199,7 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       best = b2;
     }
     // the popped entry and the new row
-    const float sc = bcast(f_sc, best), psc = bcast(f_psc, best);
+    const float sc = bcast<kSlots>(f_sc, best), psc = bcast<kSlots>(f_psc, best);
     if (adaptive) {
       const float acc1 = __fadd_rn(acc, sc);
       if (!(__fmul_rn(acc1, s.cost[row - 1]) > __fmul_rn(acc, s.cost[row]))) {
@@ -204,16 +208,17 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       }
       acc = acc1;
     }
-    const int d = bcast(f_d, best), par = bcast(f_par, best), rk = bcast(f_rk, best);
-    const uint64_t w0 = bcast(f_w0, best), w1 = bcast(f_w1, best);
-    const uint64_t pm = bcast(f_pm, best);
+    const int d = bcast<kSlots>(f_d, best), par = bcast<kSlots>(f_par, best);
+    const int rk = bcast<kSlots>(f_rk, best);
+    const uint64_t w0 = bcast<kSlots>(f_w0, best), w1 = bcast<kSlots>(f_w1, best);
+    const uint64_t pm = bcast<kSlots>(f_pm, best);
     const uint64_t m = pm | (1ull << (row - 1));
     const int rl = row & 31, rj = row >> 5;
-    put(r_sc, rj, sc, lane == rl);
-    put(r_par, rj, par, lane == rl);
-    put(r_tok, rj, s.ti[d - 1][rk], lane == rl);
-    put(r_dep, rj, d, lane == rl);
-    put(r_mask, rj, m, lane == rl);
+    put<kSlots>(r_sc, rj, sc, lane == rl);
+    put<kSlots>(r_par, rj, par, lane == rl);
+    put<kSlots>(r_tok, rj, s.ti[d - 1][rk], lane == rl);
+    put<kSlots>(r_dep, rj, d, lane == rl);
+    put<kSlots>(r_mask, rj, m, lane == rl);
     // the popped slot becomes the next sibling, or takes the last entry
     const int bl = best & 31, bj = best >> 5;
     const int last = nf - 1;
@@ -222,18 +227,20 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       uint64_t nw0 = w0, nw1 = w1;
       tuple_add(nw0, nw1, d - 1, 1ull);
       const bool me = lane == bl;
-      put(f_sc, bj, nsc, me); put(f_rk, bj, rk + 1, me);
-      put(f_w0, bj, nw0, me); put(f_w1, bj, nw1, me);
-      put(f_key, bj, primary_key(nsc, d, nw0), me);
+      put<kSlots>(f_sc, bj, nsc, me); put<kSlots>(f_rk, bj, rk + 1, me);
+      put<kSlots>(f_w0, bj, nw0, me); put<kSlots>(f_w1, bj, nw1, me);
+      put<kSlots>(f_key, bj, primary_key(nsc, d, nw0), me);
     } else {
-      const float lsc = bcast(f_sc, last), lps = bcast(f_psc, last);
-      const int ld = bcast(f_d, last), lp = bcast(f_par, last), lr = bcast(f_rk, last);
-      const uint64_t l0 = bcast(f_w0, last), l1 = bcast(f_w1, last), lk = bcast(f_key, last);
-      const uint64_t lm = bcast(f_pm, last);
+      const float lsc = bcast<kSlots>(f_sc, last), lps = bcast<kSlots>(f_psc, last);
+      const int ld = bcast<kSlots>(f_d, last), lp = bcast<kSlots>(f_par, last);
+      const int lr = bcast<kSlots>(f_rk, last);
+      const uint64_t l0 = bcast<kSlots>(f_w0, last), l1 = bcast<kSlots>(f_w1, last);
+      const uint64_t lk = bcast<kSlots>(f_key, last);
+      const uint64_t lm = bcast<kSlots>(f_pm, last);
       const bool me = lane == bl;
-      put(f_sc, bj, lsc, me); put(f_psc, bj, lps, me); put(f_d, bj, ld, me);
-      put(f_par, bj, lp, me); put(f_rk, bj, lr, me); put(f_w0, bj, l0, me);
-      put(f_w1, bj, l1, me); put(f_key, bj, lk, me); put(f_pm, bj, lm, me);
+      put<kSlots>(f_sc, bj, lsc, me); put<kSlots>(f_psc, bj, lps, me); put<kSlots>(f_d, bj, ld, me);
+      put<kSlots>(f_par, bj, lp, me); put<kSlots>(f_rk, bj, lr, me); put<kSlots>(f_w0, bj, l0, me);
+      put<kSlots>(f_w1, bj, l1, me); put<kSlots>(f_key, bj, lk, me); put<kSlots>(f_pm, bj, lm, me);
       nf = last;
     }
     // first child (rank 0 at the next position)
@@ -241,10 +248,11 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       const float csc = __fmul_rn(sc, s.tp[d][0]);
       const bool me = lane == (nf & 31);
       const int cj = nf >> 5;
-      put(f_sc, cj, csc, me); put(f_psc, cj, sc, me); put(f_d, cj, d + 1, me);
-      put(f_par, cj, row, me); put(f_rk, cj, 0, me); put(f_w0, cj, w0, me);
-      put(f_w1, cj, w1, me); put(f_pm, cj, m, me);
-      put(f_key, cj, primary_key(csc, d + 1, w0), me);
+      put<kSlots>(f_sc, cj, csc, me); put<kSlots>(f_psc, cj, sc, me);
+      put<kSlots>(f_d, cj, d + 1, me);
+      put<kSlots>(f_par, cj, row, me); put<kSlots>(f_rk, cj, 0, me); put<kSlots>(f_w0, cj, w0, me);
+      put<kSlots>(f_w1, cj, w1, me); put<kSlots>(f_pm, cj, m, me);
+      put<kSlots>(f_key, cj, primary_key(csc, d + 1, w0), me);
       ++nf;
     }
   }
@@ -317,9 +325,11 @@ tsd_status tree_build_impl(const float* probs, int B, int S, int V, int k, int D
   uint64_t* part = (uint64_t*)ws;
   vocab_scan_kernel<false><<<(unsigned)ctas, kScanThreads, 0, st>>>(probs, V, k, g.nchunk,
                                                                     g.chunk_len, part);
-  best_first_tree_kernel<<<B, 32 * S, 0, st>>>(part, S, k, D, g.nchunk, root_tok, token, parent,
-                                               depth, score, mask, is_leaf, cost_d, cost_v,
-                                               n_nodes);
+  const auto tree_kernel = D + 2 <= 32   ? best_first_tree_kernel<1>
+                           : D + 2 <= 64 ? best_first_tree_kernel<2>
+                                         : best_first_tree_kernel<3>;
+  tree_kernel<<<B, 32 * S, 0, st>>>(part, S, k, D, g.nchunk, root_tok, token, parent, depth,
+                                    score, mask, is_leaf, cost_d, cost_v, n_nodes);
   return cuda_status();
 }
 

@@ -52,7 +52,7 @@ template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloa
 // keys of split sp (and the tree rows if sp is the request's last split).
 template <typename T, int DK, int DV, int RB, bool ALIAS>
 __global__ void __launch_bounds__(kGenThreads)
-verify_generic_kernel(VerifyArgs a) {
+verify_generic_kernel(const __grid_constant__ VerifyArgs a) {
   constexpr int NK = DK / 32, NV = DV / 32;
   __shared__ float sm_m[kGenWarps][RB], sm_l[kGenWarps][RB];
   __shared__ float sm_o[kGenWarps][RB][DV];

@@ -74,6 +74,19 @@ __device__ __forceinline__ long kv_row(const VerifyArgs& a, int b, int hk, int p
   return ((long)pg * a.Hkv + hk) * a.page_size + pos % a.page_size;
 }
 
+// First row of a 128-key prefix tile in a page pool (a tile never crosses a
+// page: page sizes are multiples of 128); a page outside the pool is reported
+// and row 0 is returned so the copy stays in bounds.  Kept out of line so the
+// contiguous path's TMA issue loop is unchanged.
+__device__ __noinline__ int paged_tile_row(const VerifyArgs& a, int b, int hk, int pos) {
+  const long row = kv_row(a, b, hk, pos);
+  if (row < 0) {
+    report_error(a.err, TSD_DEV_ERR_BAD_PAGE, b);
+    return 0;
+  }
+  return (int)row;
+}
+
 template <typename T> __device__ __forceinline__ T cvt_out(float x);
 template <> __device__ __forceinline__ float cvt_out<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(float x) {
@@ -90,7 +103,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // Each split s left a normalised output O_s and its log2-sum-exp L_s; the
 // result is sum_s 2^(L_s - L) O_s with L = log2 sum_s 2^(L_s).
 template <typename T, int DV>
-__global__ void __launch_bounds__(128) verify_combine_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(128)
+verify_combine_kernel(const __grid_constant__ VerifyArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long row = (long)blockIdx.x * 4 + warp;  // ((b*R + r)*Hq + h)
   if (row >= (long)a.B * a.R * a.Hq) return;

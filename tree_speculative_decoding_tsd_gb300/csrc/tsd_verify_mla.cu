@@ -61,6 +61,7 @@ constexpr uint32_t kBox = 2 * kPiece;           // one ring slot
 constexpr int kSlots = 4;
 constexpr uint32_t kOffRing = 0;
 constexpr uint32_t kOffQ = kOffRing + kSlots * kBox;
+constexpr int kPagedTiles = 64;  // paged cache: tile rows resolved at set-up
 constexpr float kOverflow = 8.0f;               // log2 headroom of the lazy max
 constexpr int kPrefetch = 2;                    // prefix tiles prefetched into L2 ahead
 
@@ -80,7 +81,8 @@ struct MlaLayout {
   static constexpr uint32_t off_bar = off_ooff + 8 * N;
   static constexpr int nbar = 16;
   static constexpr uint32_t off_flags = off_bar + 8 * nbar;
-  static constexpr uint32_t total = off_flags + 16;  // [0] tmem [1] abort [2] K seen [3] V seen
+  static constexpr uint32_t off_tiles = off_flags + 16;  // int[kPagedTiles] tile rows (paged)
+  static constexpr uint32_t total = off_tiles + 4 * kPagedTiles;  // flags: [0] tmem [1] abort [2] K seen [3] V seen
   static_assert(q_box % 1024 == 0, "Q boxes must keep 1 KB swizzle alignment");
   static_assert(off_pt % 1024 == 0, "P^T must keep 1 KB swizzle alignment");
   static_assert(total + 1024 <= 232448, "shared memory budget");
@@ -95,9 +97,10 @@ struct MlaMaps {
   CUtensorMap k, kt;
 };
 
-template <int N>
+template <int N, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
-verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_per_cta) {
+verify_mla_kernel(const __grid_constant__ MlaMaps maps, const __grid_constant__ VerifyArgs a,
+                  int rows_per_cta) {
   using L = MlaLayout<N>;
   constexpr int NH = L::NH;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -162,15 +165,18 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_p
     return true;
   };
 
-  // first row of prefix tile t (a tile never crosses a page: page sizes are
-  // multiples of 128); a page outside the pool reads row 0 and is reported
+  // first row of prefix tile t in the cache, or in the page pool
+  // paged cache: the set-up resolves the first kPagedTiles tile rows into
+  // shared memory (tiles_ready of them, 0 until the set-up barrier)
+  int* tile_rows = (int*)(smem + L::off_tiles);
+  int tiles_ready = 0;
   auto ycoord = [&](int t) {
-    const long row = kv_row(a, b, hk, k0 + t * kKeys);
-    if (row < 0) {
-      report_error(a.err, TSD_DEV_ERR_BAD_PAGE, b);
-      return 0;
+    if constexpr (kPaged) {
+      if (t < tiles_ready) return tile_rows[t];
+      return paged_tile_row(a, b, hk, k0 + t * kKeys);
+    } else {
+      return (b * a.Hkv + hk) * a.cap + k0 + t * kKeys;
     }
-    return (int)row;
   };
   // box of pieces z, z+1 of tile t
   auto load_box = [&](uint32_t dst, int t, int z, uint32_t fb) {
@@ -234,6 +240,9 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_p
       m_run[n] = -INFINITY;
       negm[n] = 0.f;
     }
+    if constexpr (kPaged)
+      for (int t = tid; t < min(n_pre, kPagedTiles); t += kSoftWarps * 32)
+        tile_rows[t] = paged_tile_row(a, b, hk, k0 + t * kKeys);
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
@@ -241,6 +250,7 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, VerifyArgs a, int rows_p
   __syncthreads();
   fence_after();
   const uint32_t tmem = flags[0];
+  if constexpr (kPaged) tiles_ready = min(n_pre, kPagedTiles);
   const uint32_t tm_s[2] = {tmem, tmem + (uint32_t)N};
   const uint32_t tm_o = tmem + 2u * N;            // M-tile u at tm_o + u * N
   const uint32_t idesc_qk = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
@@ -633,10 +643,11 @@ bool encode_latent_tree(CUtensorMap* m, const void* base, int Hkv, long rows) {
 template <int N>
 void launch_mla(const MlaMaps& maps, const VerifyArgs& a, const VerifyPlan& p, cudaStream_t st) {
   const uint32_t smem = MlaLayout<N>::total + 1024;
-  cudaFuncSetAttribute(verify_mla_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const auto kern = a.page_size > 0 ? verify_mla_kernel<N, true> : verify_mla_kernel<N, false>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
   const dim3 grid(p.nsplit, a.Hkv * p.nrg, a.B);
-  verify_mla_kernel<N><<<grid, kThreads, smem, st>>>(maps, a, p.rb);
+  kern<<<grid, kThreads, smem, st>>>(maps, a, p.rb);
 }
 
 }  // namespace

@@ -66,7 +66,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 template <int DK>
 __global__ void __launch_bounds__(256)
-verify_mma_kernel(VerifyArgs a, int rows_per_cta) {
+verify_mma_kernel(const __grid_constant__ VerifyArgs a, int rows_per_cta) {
   constexpr int CH = DK / 8;                 // 16-byte chunks per K/V row
   constexpr int TILE_CHUNKS = kTK * CH;      // uint4 per K (or V) tile
   extern __shared__ __align__(128) uint4 smem[];

@@ -56,6 +56,7 @@ constexpr uint32_t kTileBytes = 2 * kBox;       // one K or V tile: 32 KB
 constexpr uint32_t kOffK = 0;                   // K ring: 2 x 32 KB
 constexpr uint32_t kOffV = 2 * kTileBytes;      // V ring: 2 x 32 KB
 constexpr uint32_t kOffQ = 4 * kTileBytes;      // 128 KB
+constexpr int kPagedTiles = 64;  // paged cache: tile rows resolved at set-up
 constexpr float kOverflow = 8.0f;               // log2 headroom of the lazy max
 constexpr int kPrefetch = 3;                    // prefix tiles prefetched into L2 ahead
 
@@ -77,7 +78,8 @@ struct TcLayout {
   static constexpr uint32_t off_bar = off_ooff + 8 * N;             // mbarriers
   static constexpr int nbar = 13;
   static constexpr uint32_t off_flags = off_bar + 8 * nbar;          // tmem addr, abort flag
-  static constexpr uint32_t total = off_flags + 16;
+  static constexpr uint32_t off_tiles = off_flags + 16;  // int[kPagedTiles] tile rows (paged)
+  static constexpr uint32_t total = off_tiles + 4 * kPagedTiles;
   static_assert(total + 1024 <= 232448, "shared memory budget");
 };
 
@@ -89,9 +91,10 @@ struct TcMaps {
   CUtensorMap k, v, kt, vt;
 };
 
-template <int N>
+template <int N, bool kPaged>
 __global__ void __launch_bounds__(kThreadsTC, 1)
-verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per_cta) {
+verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ VerifyArgs a,
+                 int rows_per_cta) {
   using L = TcLayout<N>;
   constexpr int NH = L::NH;
   // 128-byte-swizzled TMA boxes and MMA operands need 1024-byte-aligned atoms:
@@ -126,15 +129,18 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
   // ---------------------------------------------------------------- set-up
   // The TMA thread initialises the barriers and starts the first loads at
   // once, so they overlap the Q staging and the TMEM allocation.
-  // first row of prefix tile t (a tile never crosses a page: page sizes are
-  // multiples of 128); a page outside the pool reads row 0 and is reported
+  // first row of prefix tile t in the cache, or in the page pool
+  // paged cache: the set-up resolves the first kPagedTiles tile rows into
+  // shared memory (tiles_ready of them, 0 until the set-up barrier)
+  int* tile_rows = (int*)(smem + L::off_tiles);
+  int tiles_ready = 0;
   auto ycoord = [&](int t) {
-    const long row = kv_row(a, b, hk, k0 + t * kKeys);
-    if (row < 0) {
-      report_error(a.err, TSD_DEV_ERR_BAD_PAGE, b);
-      return 0;
+    if constexpr (kPaged) {
+      if (t < tiles_ready) return tile_rows[t];
+      return paged_tile_row(a, b, hk, k0 + t * kKeys);
+    } else {
+      return (b * a.Hkv + hk) * a.cap + k0 + t * kKeys;
     }
-    return (int)row;
   };
   auto tma_k = [&](int t, int stage) {
     const uint32_t dst = sbase + kOffK + stage * kTileBytes;
@@ -219,6 +225,9 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
       m_run[n] = -INFINITY;
       negm[n] = 0.f;
     }
+    if constexpr (kPaged)
+      for (int t = tid; t < min(n_pre, kPagedTiles); t += kSoftWarps * 32)
+        tile_rows[t] = paged_tile_row(a, b, hk, k0 + t * kKeys);
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
@@ -226,6 +235,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, VerifyArgs a, int rows_per
   __syncthreads();
   fence_after();
   const uint32_t tmem = flags[0];
+  if constexpr (kPaged) tiles_ready = min(n_pre, kPagedTiles);
   const uint32_t tm_s[2] = {tmem, tmem + (uint32_t)N};
   const uint32_t tm_o = tmem + 2u * N;
 
@@ -576,9 +586,10 @@ bool encode_3d(CUtensorMap* m, const void* base, int Hkv, long rows) {
 template <int N>
 void launch_tc(const TcMaps& maps, const VerifyArgs& a, const VerifyPlan& p, cudaStream_t st) {
   const uint32_t smem = TcLayout<N>::total + 1024;
-  cudaFuncSetAttribute(verify_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const auto kern = a.page_size > 0 ? verify_tc_kernel<N, true> : verify_tc_kernel<N, false>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const dim3 grid(p.nsplit, a.Hkv * p.nrg, a.B);
-  verify_tc_kernel<N><<<grid, kThreadsTC, smem, st>>>(maps, a, p.rb);
+  kern<<<grid, kThreadsTC, smem, st>>>(maps, a, p.rb);
 }
 
 }  // namespace
