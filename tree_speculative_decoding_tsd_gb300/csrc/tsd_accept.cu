@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kMaxR = 65;
 
-constexpr int kWalkWarps = 8;
+constexpr int kWalkWarps = 32;   // one warp per tree row up to 32 rows: their chunk loads overlap
 
 __global__ void __launch_bounds__(32 * kWalkWarps)
 accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
@@ -35,6 +35,7 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
                    int32_t* __restrict__ tgt_out, int32_t* __restrict__ accept_len,
                    int32_t* __restrict__ accept_rows, int32_t* __restrict__ bonus,
                    int32_t* __restrict__ chain_id, int32_t* __restrict__ err) {
+  grid_dependency_sync();
   __shared__ int32_t s_tgt[kMaxR], s_tok[kMaxR], s_par[kMaxR];
   __shared__ uint64_t s_mask[kMaxR];
   __shared__ uint8_t s_leaf[kMaxR];
@@ -42,8 +43,15 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long o = (long)b * R;
 
-  // tgt[r]: the largest of the row's chunk maxima.  Warp w takes rows w, w+8,
-  // ...; its lanes split the (at most 256) chunks and load them all at once.
+  // tree metadata, then tgt[r]: the largest of the row's chunk maxima.  Warp
+  // w takes rows w, w+32, ...; its lanes split the (at most 256) chunks and
+  // load them all at once.
+  for (int r = threadIdx.x; r < R; r += 32 * kWalkWarps) {
+    s_tok[r] = token[o + r];
+    s_par[r] = parent[o + r];
+    s_mask[r] = mask[o + r];
+    s_leaf[r] = is_leaf[o + r];
+  }
   for (int r = warp; r < R; r += kWalkWarps) {
     const uint64_t* src = part + (o + r) * nchunk;
     uint64_t c[kScanMaxCand / 32];
@@ -61,12 +69,6 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
       s_tgt[r] = t;
       if (tgt_out != nullptr) tgt_out[o + r] = t;
     }
-  }
-  for (int r = threadIdx.x; r < R; r += 32 * kWalkWarps) {
-    s_tok[r] = token[o + r];
-    s_par[r] = parent[o + r];
-    s_mask[r] = mask[o + r];
-    s_leaf[r] = is_leaf[o + r];
   }
   __syncthreads();
   if (warp != 0) return;
@@ -156,10 +158,10 @@ extern "C" tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, 
   const long rows = (long)B * R;
   const ScanGeom g = scan_geometry(rows, V, 1, true);
   uint64_t* part = (uint64_t*)ws;
-  vocab_scan_kernel<true><<<(unsigned)(rows * g.nchunk), kScanThreads, 0, st>>>(
+  launch(vocab_scan_kernel<true>, dim3((unsigned)(rows * g.nchunk)), dim3(kScanThreads), 0, st,
       logits, V, 1, g.nchunk, g.chunk_len, part);
-  accept_walk_kernel<<<B, 32 * kWalkWarps, 0, st>>>(part, R, S, g.nchunk, token, parent, mask, is_leaf, tgt,
-                                       accept_len, accept_rows, bonus, chain_id, err);
+  launch(accept_walk_kernel, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk, token,
+      parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err);
   return cuda_status();
 }
 
@@ -226,9 +228,9 @@ extern "C" tsd_status tsd_accept_walk_static(const float* logits, int B, int D, 
   const int R = D + 1;
   const long rows = (long)B * R;
   const ScanGeom g = scan_geometry(rows, V, 1, true);
-  vocab_scan_kernel<true><<<(unsigned)(rows * g.nchunk), kScanThreads, 0, st>>>(
+  launch(vocab_scan_kernel<true>, dim3((unsigned)(rows * g.nchunk)), dim3(kScanThreads), 0, st,
       logits, V, 1, g.nchunk, g.chunk_len, part);
-  accept_walk_kernel<<<B, 32 * kWalkWarps, 0, st>>>(part, R, S, g.nchunk, token, parent, mask, is_leaf, tgt,
-                                       accept_len, accept_rows, bonus, chain_id, err);
+  launch(accept_walk_kernel, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk, token,
+      parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err);
   return cuda_status();
 }

@@ -8,18 +8,21 @@
 // the next round starts from the extended prefix.  (Token-level KV refresh is
 // all a sliding-window / dense cache needs.)
 //
-// K6 commit_path_kernel: one CTA per request.  Its threads split the (row,
-// head, K|V, 16-byte vector) copies; every thread reads the old prefix length
-// before the block barrier and thread 0 writes the new one after it.  (At most
-// (S+1) x Hkv rows of a few KB move per request: one CTA is enough, and a
-// cluster's launch and barrier cost more than they save.)
+// K6 commit_path_kernel: one CTA per request.  Thread 0 reads the prefix and
+// path lengths once for the CTA (and writes the new prefix length at the end);
+// thread i checks path entry i and resolves its cache row; then the threads
+// split the (row, head, K|V, 16-byte vector) copies, kCommitUnroll loads in
+// flight each.  (At most (S+1) x Hkv rows of a few KB move per
+// request: one CTA is enough, and a cluster's launch and barrier cost more
+// than they save.)
 #include "tsd_common.cuh"
 #include "tsd_host.h"
 
 namespace tsd {
 namespace {
 
-constexpr int kCommitThreads = 256;
+constexpr int kCommitThreads = 512;
+constexpr int kCommitMaxRows = 17;   // 1 + S, S <= 16
 
 struct CommitArgs {
   const char* ktree;
@@ -39,54 +42,88 @@ struct CommitArgs {
   int max_pages, page_size, num_pages;
 };
 
-// Cache row of position pos of (request b, head h); -1 for a page outside the pool.
-__device__ __forceinline__ long cache_row(const CommitArgs& a, int b, int h, int pos) {
-  if (a.page_size == 0) return ((long)b * a.Hkv + h) * a.cap + pos;
+// Cache row of position pos of (request b, head 0), and the row stride between
+// heads; -1 for a page outside the pool.
+__device__ __forceinline__ long cache_row0(const CommitArgs& a, int b, int pos) {
+  if (a.page_size == 0) return (long)b * a.Hkv * a.cap + pos;
   const int pg = a.page_table[(long)b * a.max_pages + pos / a.page_size];
   if (pg < 0 || pg >= a.num_pages) return -1;
-  return ((long)pg * a.Hkv + h) * a.page_size + pos % a.page_size;
+  return (long)pg * a.Hkv * a.page_size + pos % a.page_size;
 }
 
-__global__ void __launch_bounds__(kCommitThreads) commit_path_kernel(CommitArgs a) {
-  const int b = blockIdx.x;
-  const int P = a.prefix_len[b];
-  const int L = a.accept_len[b];
-  const int32_t* rows = a.accept_rows + (long)b * (a.S + 1);
+constexpr int kCommitUnroll = 4;   // 16-byte loads in flight per thread
+constexpr int kNoError = 0x7fffffff;   // above every TSD_DEV_ERR_* code
 
+__global__ void __launch_bounds__(kCommitThreads) commit_path_kernel(CommitArgs a) {
+  __shared__ int32_t s_src[kCommitMaxRows];   // scratch-pad row of path entry i
+  __shared__ long s_dst[kCommitMaxRows];      // cache row of position P + i, head 0
+  __shared__ int s_P, s_L, s_code;
+  grid_dependency_sync();
+  const int b = blockIdx.x, tid = threadIdx.x;
+  // one read of the prefix and path lengths, shared by the whole CTA
+  if (tid == 0) {
+    s_P = a.prefix_len[b];
+    s_L = a.accept_len[b];
+    s_code = kNoError;
+  }
+  __syncthreads();
+  const int P = s_P, L = s_L;
+
+  // validation: thread i checks path entry i (row index, page of P + i)
   int code = 0;
   if (L < 0 || L > a.S) code = TSD_DEV_ERR_BAD_TREE;
   else if (P < 0 || (long)P + 1 + L > a.cap) code = TSD_DEV_ERR_CAPACITY;
-  else
-    for (int i = 0; i <= L; ++i) {
-      if (rows[i] < 0 || rows[i] >= a.R) code = TSD_DEV_ERR_BAD_TREE;
-      else if (cache_row(a, b, 0, P + i) < 0) code = TSD_DEV_ERR_BAD_PAGE;
-    }
+  else if (tid <= L) {
+    const int r = a.accept_rows[(long)b * (a.S + 1) + tid];
+    const long d0 = cache_row0(a, b, P + tid);
+    if (r < 0 || r >= a.R) code = TSD_DEV_ERR_BAD_TREE;
+    else if (d0 < 0) code = TSD_DEV_ERR_BAD_PAGE;
+    s_src[tid] = r;
+    s_dst[tid] = d0;
+  }
+  // one code for the request: the smallest one any thread found
+  if (code != 0) atomicMin(&s_code, code);
+  __syncthreads();
+  code = s_code == kNoError ? 0 : s_code;
 
   if (code == 0) {
     const int per_head = a.kvec + a.vvec;
-    const long work = (long)(L + 1) * a.Hkv * per_head;
-    for (long w = threadIdx.x; w < work; w += kCommitThreads) {
-      const int i = (int)(w / ((long)a.Hkv * per_head));
-      const int rem = (int)(w - (long)i * a.Hkv * per_head);
-      const int h = rem / per_head;
-      const int e = rem - h * per_head;
-      const long src_row = ((long)b * a.R + rows[i]) * a.Hkv + h;
-      const long dst_row = cache_row(a, b, h, P + i);
-      const int4* src;
-      int4* dst;
-      if (e < a.kvec) {
-        src = reinterpret_cast<const int4*>(a.ktree + src_row * a.krow) + e;
-        dst = reinterpret_cast<int4*>(a.kcache + dst_row * a.krow) + e;
-      } else {
-        src = reinterpret_cast<const int4*>(a.vtree + src_row * a.vrow) + (e - a.kvec);
-        dst = reinterpret_cast<int4*>(a.vcache + dst_row * a.vrow) + (e - a.kvec);
+    const int per_row = a.Hkv * per_head;
+    const int work = (L + 1) * per_row;
+    const long hstride = a.page_size ? a.page_size : a.cap;
+    for (int w0 = tid; w0 < work; w0 += kCommitThreads * kCommitUnroll) {
+      // all loads of the batch first, then the stores (the stores could alias
+      // the sources as far as the compiler knows)
+      int4 v[kCommitUnroll];
+      int4* dst[kCommitUnroll];
+#pragma unroll
+      for (int u = 0; u < kCommitUnroll; ++u) {
+        const int w = w0 + u * kCommitThreads;
+        dst[u] = nullptr;
+        if (w < work) {
+          const int i = w / per_row;
+          const int rem = w - i * per_row;
+          const int h = rem / per_head;
+          const int e = rem - h * per_head;
+          const long src_row = ((long)b * a.R + s_src[i]) * a.Hkv + h;
+          const long dst_row = s_dst[i] + h * hstride;
+          const int4* src;
+          if (e < a.kvec) {
+            src = reinterpret_cast<const int4*>(a.ktree + src_row * a.krow) + e;
+            dst[u] = reinterpret_cast<int4*>(a.kcache + dst_row * a.krow) + e;
+          } else {
+            src = reinterpret_cast<const int4*>(a.vtree + src_row * a.vrow) + (e - a.kvec);
+            dst[u] = reinterpret_cast<int4*>(a.vcache + dst_row * a.vrow) + (e - a.kvec);
+          }
+          v[u] = __ldg(src);
+        }
       }
-      *dst = __ldg(src);
+#pragma unroll
+      for (int u = 0; u < kCommitUnroll; ++u)
+        if (dst[u] != nullptr) *dst[u] = v[u];
     }
   }
-  // every thread has read prefix_len[b] before anyone passes this barrier
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     if (code == 0) a.prefix_len[b] = P + 1 + L;
     else report_error(a.err, code, b);
   }
@@ -142,7 +179,7 @@ static tsd_status commit_impl(const tsd_attn_desc* d, int S, const void* ktree, 
   a.max_pages = paged ? max_pages : 0;
   a.page_size = paged ? page_size : 0;
   a.num_pages = paged ? num_pages : 0;
-  commit_path_kernel<<<d->B, kCommitThreads, 0, (cudaStream_t)stream>>>(a);
+  launch(commit_path_kernel, dim3(d->B), dim3(kCommitThreads), 0, (cudaStream_t)stream, a);
   return cuda_status();
 }
 

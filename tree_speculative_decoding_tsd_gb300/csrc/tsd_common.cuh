@@ -35,6 +35,18 @@ __device__ __forceinline__ uint64_t make_cand(float x, uint32_t id) {
 __device__ __forceinline__ uint32_t cand_id(uint64_t c) { return ~(uint32_t)c; }
 __device__ __forceinline__ float cand_val(uint64_t c) { return order_key_f32((uint32_t)(c >> 32)); }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation (tsd::launch in tsd_host.h) may be scheduled while the kernel
+// before it on the stream is still running.  Before its first global read or
+// write each thread waits until that kernel has completed and its writes are
+// visible (a no-op after an ordinary launch); then the CTA lets the next
+// kernel be scheduled (its set-up overlaps this kernel's work).  Only set-up
+// that touches no global memory may precede this call.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // First device error wins; request index in the low 24 bits.
 __device__ __forceinline__ void report_error(int32_t* err, int code, int b) {
   if (err != nullptr) atomicCAS(err, 0, code | (b & 0xffffff));

@@ -70,6 +70,7 @@ template <bool kArgmax>
 __global__ void __launch_bounds__(kScanThreads, kArgmax ? kScanArgmaxPerSm : kScanTopkPerSm)
 vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chunk_len,
                   uint64_t* __restrict__ out) {
+  grid_dependency_sync();
   __shared__ uint64_t s_list[kScanWarps][32];
   __shared__ float s_max[kScanThreads];
   __shared__ float s_cut;

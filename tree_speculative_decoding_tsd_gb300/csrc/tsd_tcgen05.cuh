@@ -81,6 +81,12 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, i
                "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// Bring a tensor map (a __grid_constant__ kernel parameter) into the
+// descriptor cache ahead of its first copy.
+__device__ __forceinline__ void tma_desc_prefetch(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"((uint64_t)map) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(map),
                "r"(x), "r"(y)

@@ -94,6 +94,7 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
                        float* __restrict__ score, uint64_t* __restrict__ mask,
                        uint8_t* __restrict__ is_leaf, const float* __restrict__ cost_d,
                        const float* __restrict__ cost_v, int32_t* __restrict__ n_nodes) {
+  grid_dependency_sync();
   __shared__ TreeSmem s;
   const int b = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -323,13 +324,13 @@ tsd_status tree_build_impl(const float* probs, int B, int S, int V, int k, int D
   const ScanGeom g = scan_geometry((long)B * S, V, k, false);
   const long ctas = (long)B * S * g.nchunk;
   uint64_t* part = (uint64_t*)ws;
-  vocab_scan_kernel<false><<<(unsigned)ctas, kScanThreads, 0, st>>>(probs, V, k, g.nchunk,
-                                                                    g.chunk_len, part);
+  launch(vocab_scan_kernel<false>, dim3((unsigned)ctas), dim3(kScanThreads), 0, st, probs, V, k,
+      g.nchunk, g.chunk_len, part);
   const auto tree_kernel = D + 2 <= 32   ? best_first_tree_kernel<1>
                            : D + 2 <= 64 ? best_first_tree_kernel<2>
                                          : best_first_tree_kernel<3>;
-  tree_kernel<<<B, 32 * S, 0, st>>>(part, S, k, D, g.nchunk, root_tok, token, parent, depth,
-                                    score, mask, is_leaf, cost_d, cost_v, n_nodes);
+  launch(tree_kernel, dim3(B), dim3(32 * S), 0, st, part, S, k, D, g.nchunk, root_tok, token,
+      parent, depth, score, mask, is_leaf, cost_d, cost_v, n_nodes);
   return cuda_status();
 }
 

@@ -35,6 +35,7 @@ conditioned_tree_kernel(const float* __restrict__ cand_p, const int32_t* __restr
                         int32_t* __restrict__ parent, int32_t* __restrict__ depth,
                         float* __restrict__ score, uint64_t* __restrict__ mask,
                         uint8_t* __restrict__ is_leaf, int32_t* __restrict__ err) {
+  grid_dependency_sync();
   __shared__ uint64_t key[kCondMaxCand];
   __shared__ float sc[kCondMaxCand];
   __shared__ int32_t par[kCondMaxCand];
@@ -202,8 +203,7 @@ extern "C" tsd_status tsd_tree_build_conditioned(const float* cand_p, const int3
       !ok_ptr(token) || !ok_ptr(parent) || !ok_ptr(depth) || !ok_ptr(score) || !ok_ptr(mask) ||
       !ok_ptr(is_leaf) || !ok_opt_ptr(err))
     return TSD_ERR_INVALID_ARG;
-  conditioned_tree_kernel<<<B, kCondThreads, 0, (cudaStream_t)stream>>>(
-      cand_p, cand_tok, cand_parent, C, D, root_tok, token, parent, depth, score, mask, is_leaf,
-      err);
+  launch(conditioned_tree_kernel, dim3(B), dim3(kCondThreads), 0, (cudaStream_t)stream, cand_p,
+      cand_tok, cand_parent, C, D, root_tok, token, parent, depth, score, mask, is_leaf, err);
   return cuda_status();
 }

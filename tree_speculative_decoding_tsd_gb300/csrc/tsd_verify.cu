@@ -53,6 +53,7 @@ template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloa
 template <typename T, int DK, int DV, int RB, bool ALIAS>
 __global__ void __launch_bounds__(kGenThreads)
 verify_generic_kernel(const __grid_constant__ VerifyArgs a) {
+  grid_dependency_sync();
   constexpr int NK = DK / 32, NV = DV / 32;
   __shared__ float sm_m[kGenWarps][RB], sm_l[kGenWarps][RB];
   __shared__ float sm_o[kGenWarps][RB][DV];
@@ -250,10 +251,11 @@ VerifyPlan plan_verify(const tsd_attn_desc& d) {
 template <typename T, int DK, int DV, int RB, bool ALIAS>
 static void launch_generic(const VerifyArgs& a, const VerifyPlan& p, cudaStream_t st) {
   const dim3 grid(p.nsplit, a.Hkv * p.nrg, a.B);
-  verify_generic_kernel<T, DK, DV, RB, ALIAS><<<grid, kGenThreads, 0, st>>>(a);
+  launch(verify_generic_kernel<T, DK, DV, RB, ALIAS>, dim3(grid), dim3(kGenThreads), 0, st, a);
   if (p.nsplit > 1) {
     const long rows = (long)a.B * a.R * a.Hq;
-    verify_combine_kernel<T, DV><<<(unsigned)ceil_div(rows, 4), 128, 0, st>>>(a);
+    launch_plain(verify_combine_kernel<T, DV>, dim3((unsigned)ceil_div(rows, 4)), dim3(128), 0,
+                 st, a);
   }
 }
 

@@ -99,20 +99,13 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Merge the per-split partials of every output row: one warp per (b, r, h).
+// Merge the nsb split partials of one output row (b, r, h) with one warp.
 // Each split s left a normalised output O_s and its log2-sum-exp L_s; the
 // result is sum_s 2^(L_s - L) O_s with L = log2 sum_s 2^(L_s).
 template <typename T, int DV>
-__global__ void __launch_bounds__(128)
-verify_combine_kernel(const __grid_constant__ VerifyArgs a) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long row = (long)blockIdx.x * 4 + warp;  // ((b*R + r)*Hq + h)
-  if (row >= (long)a.B * a.R * a.Hq) return;
-  const int b = (int)(row / ((long)a.R * a.Hq));
-  const int r = (int)((row / a.Hq) % a.R);
-  const int h = (int)(row % a.Hq);
-  const int P = min(max(a.plen[b], 0), a.cap);
-  const int nsb = P > 0 ? (P + a.split_len - 1) / a.split_len : 1;
+__device__ __forceinline__ void merge_splits(const VerifyArgs& a, int b, int r, int h, int nsb,
+                                             int lane) {
+  const long row = ((long)b * a.R + r) * a.Hq + h;
   const long base = (((long)b * a.Hq + h) * a.R + r) * a.nsplit;
   float mx = -INFINITY;
   for (int s = lane; s < nsb; s += 32) mx = fmaxf(mx, a.ws_lse[base + s]);
@@ -123,18 +116,61 @@ verify_combine_kernel(const __grid_constant__ VerifyArgs a) {
   sum = warp_sum(sum);
   const float tot = mx + log2f(sum);
   constexpr int NV = DV / 32;
+  constexpr int kU = 4;  // partials in flight per lane: NV * kU loads
   float acc[NV];
 #pragma unroll
   for (int t = 0; t < NV; ++t) acc[t] = 0.f;
-  for (int s = 0; s < nsb; ++s) {
-    const float w = exp2f(a.ws_lse[base + s] - tot);
-    const float* src = a.ws_o + (base + s) * DV;
+  // acc = sum over s in increasing order of fma(w_s, O_s, acc); lane j of a
+  // round of 32 splits holds w_(s0+j), and the loads of kU partials are issued
+  // before their products
+  for (int s0 = 0; s0 < nsb; s0 += 32) {
+    const int n = min(32, nsb - s0);
+    const float wl = lane < n ? exp2f(a.ws_lse[base + s0 + lane] - tot) : 0.f;
+    const float* src = a.ws_o + (base + s0) * DV + lane;
+    int j = 0;
+    for (; j + kU <= n; j += kU) {
+      float x[kU][NV];
 #pragma unroll
-    for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, src[lane + 32 * t], acc[t]);
+      for (int u = 0; u < kU; ++u)
+#pragma unroll
+        for (int t = 0; t < NV; ++t) x[u][t] = src[(j + u) * DV + 32 * t];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const float w = __shfl_sync(kFull, wl, j + u);
+#pragma unroll
+        for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, x[u][t], acc[t]);
+      }
+    }
+    for (; j < n; ++j) {
+      const float w = __shfl_sync(kFull, wl, j);
+#pragma unroll
+      for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, src[j * DV + 32 * t], acc[t]);
+    }
   }
 #pragma unroll
   for (int t = 0; t < NV; ++t) ((T*)a.out)[row * DV + lane + 32 * t] = cvt_out<T>(acc[t]);
   if (lane == 0) a.lse[row] = tot * 0.69314718055994531f;
+}
+
+// Split merge: one warp per output row ((b*R + r)*Hq + h), spread over the
+// whole GPU (merging in the last CTA of each request and head instead left
+// one CTA with a serial tail of dependent loads: 10% slower attention on every
+// workload).  It is launched with ordinary stream serialisation: launched
+// early next to a multi-wave attention grid, its CTAs slowed the following
+// kernels (5% on the batched step).
+template <typename T, int DV>
+__global__ void __launch_bounds__(128)
+verify_combine_kernel(const __grid_constant__ VerifyArgs a) {
+  grid_dependency_sync();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long row = (long)blockIdx.x * 4 + warp;
+  if (row >= (long)a.B * a.R * a.Hq) return;
+  const int b = (int)(row / ((long)a.R * a.Hq));
+  const int r = (int)((row / a.Hq) % a.R);
+  const int h = (int)(row % a.Hq);
+  const int P = min(max(a.plen[b], 0), a.cap);
+  const int nsb = P > 0 ? (P + a.split_len - 1) / a.split_len : 1;
+  merge_splits<T, DV>(a, b, r, h, nsb, lane);
 }
 
 }  // namespace

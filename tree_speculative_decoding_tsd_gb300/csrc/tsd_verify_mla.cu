@@ -102,6 +102,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 verify_mla_kernel(const __grid_constant__ MlaMaps maps, const __grid_constant__ VerifyArgs a,
                   int rows_per_cta) {
   using L = MlaLayout<N>;
+  if (threadIdx.x == kTmaWarp0 * 32) {
+    tma_desc_prefetch(&maps.k);
+    tma_desc_prefetch(&maps.kt);
+  }
+  grid_dependency_sync();
   constexpr int NH = L::NH;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = su32(smem_raw);
@@ -647,7 +652,7 @@ void launch_mla(const MlaMaps& maps, const VerifyArgs& a, const VerifyPlan& p, c
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
   const dim3 grid(p.nsplit, a.Hkv * p.nrg, a.B);
-  kern<<<grid, kThreads, smem, st>>>(maps, a, p.rb);
+  launch(kern, dim3(grid), dim3(kThreads), smem, st, maps, a, p.rb);
 }
 
 }  // namespace
@@ -665,7 +670,8 @@ bool launch_mla_tc_path(const tsd_attn_desc& d, const VerifyArgs& a, const Verif
   launch_mla<64>(maps, a, p, st);
   if (p.nsplit > 1) {
     const long rows = (long)a.B * a.R * a.Hq;
-    verify_combine_kernel<__nv_bfloat16, kDV><<<(unsigned)ceil_div(rows, 4), 128, 0, st>>>(a);
+    launch_plain(verify_combine_kernel<__nv_bfloat16, kDV>, dim3((unsigned)ceil_div(rows, 4)),
+                 dim3(128), 0, st, a);
   }
   return true;
 }

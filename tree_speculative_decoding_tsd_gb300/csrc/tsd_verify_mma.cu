@@ -67,6 +67,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 template <int DK>
 __global__ void __launch_bounds__(256)
 verify_mma_kernel(const __grid_constant__ VerifyArgs a, int rows_per_cta) {
+  grid_dependency_sync();
   constexpr int CH = DK / 8;                 // 16-byte chunks per K/V row
   constexpr int TILE_CHUNKS = kTK * CH;      // uint4 per K (or V) tile
   extern __shared__ __align__(128) uint4 smem[];
@@ -294,20 +295,22 @@ bool launch_mma_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPl
   if (d.dk == 128) {
     cudaFuncSetAttribute(verify_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
-    verify_mma_kernel<128><<<grid, threads, smem, st>>>(a, p.rb);
+    launch(verify_mma_kernel<128>, dim3(grid), dim3(threads), smem, st, a, p.rb);
   } else if (d.dk == 64) {
     cudaFuncSetAttribute(verify_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
-    verify_mma_kernel<64><<<grid, threads, smem, st>>>(a, p.rb);
+    launch(verify_mma_kernel<64>, dim3(grid), dim3(threads), smem, st, a, p.rb);
   } else {
     return false;
   }
   if (p.nsplit > 1) {
     const long rows = (long)a.B * a.R * a.Hq;
     if (d.dk == 128)
-      verify_combine_kernel<__nv_bfloat16, 128><<<(unsigned)ceil_div(rows, 4), 128, 0, st>>>(a);
+      launch_plain(verify_combine_kernel<__nv_bfloat16, 128>, dim3((unsigned)ceil_div(rows, 4)),
+                   dim3(128), 0, st, a);
     else
-      verify_combine_kernel<__nv_bfloat16, 64><<<(unsigned)ceil_div(rows, 4), 128, 0, st>>>(a);
+      launch_plain(verify_combine_kernel<__nv_bfloat16, 64>, dim3((unsigned)ceil_div(rows, 4)),
+                   dim3(128), 0, st, a);
   }
   return true;
 }

@@ -96,6 +96,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ VerifyArgs a,
                  int rows_per_cta) {
   using L = TcLayout<N>;
+  if (threadIdx.x == kTmaWarp * 32) {
+    tma_desc_prefetch(&maps.k);
+    tma_desc_prefetch(&maps.v);
+    tma_desc_prefetch(&maps.kt);
+    tma_desc_prefetch(&maps.vt);
+  }
+  grid_dependency_sync();
   constexpr int NH = L::NH;
   // 128-byte-swizzled TMA boxes and MMA operands need 1024-byte-aligned atoms:
   // align the dynamic shared-memory base by hand (1 KB of slack is requested)
@@ -589,7 +596,7 @@ void launch_tc(const TcMaps& maps, const VerifyArgs& a, const VerifyPlan& p, cud
   const auto kern = a.page_size > 0 ? verify_tc_kernel<N, true> : verify_tc_kernel<N, false>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const dim3 grid(p.nsplit, a.Hkv * p.nrg, a.B);
-  kern<<<grid, kThreadsTC, smem, st>>>(maps, a, p.rb);
+  launch(kern, dim3(grid), dim3(kThreadsTC), smem, st, maps, a, p.rb);
 }
 
 }  // namespace
@@ -621,7 +628,8 @@ bool launch_tc_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPla
   }
   if (p.nsplit > 1) {
     const long rows = (long)a.B * a.R * a.Hq;
-    verify_combine_kernel<__nv_bfloat16, 128><<<(unsigned)ceil_div(rows, 4), 128, 0, st>>>(a);
+    launch_plain(verify_combine_kernel<__nv_bfloat16, 128>, dim3((unsigned)ceil_div(rows, 4)),
+                 dim3(128), 0, st, a);
   }
   return true;
 }
