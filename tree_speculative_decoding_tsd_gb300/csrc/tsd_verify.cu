@@ -214,14 +214,16 @@ VerifyPlan plan_verify(const tsd_attn_desc& d) {
     p.nrg = (int)ceil_div(M, 144);
     p.rb = (int)ceil_div(ceil_div(M, p.nrg), 16) * 16;
     // Splits: about two waves of CTAs for the whole batch.  A split writes a
-    // partial output as large as ~130 keys of K/V, so splits stay >= 512 keys
-    // (>= 1024 once the batch alone fills the GPU) and <= 4096 keys.  The split
-    // depends on B: results are deterministic, but their rounding can differ
-    // between batch sizes.
+    // partial output as large as ~130 keys of K/V, so splits stay >= 256 keys
+    // (>= 1024 once the batch alone fills the GPU) and <= 4096 keys; for a
+    // small batch the shorter splits shorten the critical path (qwen-sized
+    // step: 256-key splits 2.5 us faster than 512).  The split depends on B:
+    // results are deterministic, but their rounding can differ between batch
+    // sizes.
     const long units = (long)d.B * d.Hkv * p.nrg;
     ns = ceil_div(152L * 2, units);
     long len = ceil_div(ceil_div(d.cap, ns), 128) * 128;  // whole 128-key tiles
-    const long lo = units >= 152 ? 1024 : 512;
+    const long lo = units >= 152 ? 1024 : 256;
     if (len < lo) len = lo;
     if (len > 4096) len = 4096;
     p.split_len = (int)len;

@@ -116,35 +116,32 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, int b, int r, 
   sum = warp_sum(sum);
   const float tot = mx + log2f(sum);
   constexpr int NV = DV / 32;
-  constexpr int kU = 4;  // partials in flight per lane: NV * kU loads
+  constexpr int kU = DV <= 128 ? 8 : 4;  // partials in flight per lane: NV * kU loads
   float acc[NV];
 #pragma unroll
   for (int t = 0; t < NV; ++t) acc[t] = 0.f;
   // acc = sum over s in increasing order of fma(w_s, O_s, acc); lane j of a
-  // round of 32 splits holds w_(s0+j), and the loads of kU partials are issued
-  // before their products
+  // round of 32 splits holds w_(s0+j)
   for (int s0 = 0; s0 < nsb; s0 += 32) {
     const int n = min(32, nsb - s0);
     const float wl = lane < n ? exp2f(a.ws_lse[base + s0 + lane] - tot) : 0.f;
     const float* src = a.ws_o + (base + s0) * DV + lane;
-    int j = 0;
-    for (; j + kU <= n; j += kU) {
+    // batches of kU partials; the loads past n are predicated off, so a row
+    // with at most kU splits (per round) takes one trip to L2
+    for (int j = 0; j < n; j += kU) {
       float x[kU][NV];
 #pragma unroll
       for (int u = 0; u < kU; ++u)
 #pragma unroll
-        for (int t = 0; t < NV; ++t) x[u][t] = src[(j + u) * DV + 32 * t];
+        for (int t = 0; t < NV; ++t) x[u][t] = j + u < n ? src[(j + u) * DV + 32 * t] : 0.f;
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        const float w = __shfl_sync(kFull, wl, j + u);
+        const float w = __shfl_sync(kFull, wl, (j + u) & 31);
+        if (j + u < n) {
 #pragma unroll
-        for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, x[u][t], acc[t]);
+          for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, x[u][t], acc[t]);
+        }
       }
-    }
-    for (; j < n; ++j) {
-      const float w = __shfl_sync(kFull, wl, j);
-#pragma unroll
-      for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, src[j * DV + 32 * t], acc[t]);
     }
   }
 #pragma unroll

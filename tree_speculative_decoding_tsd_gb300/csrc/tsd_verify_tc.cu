@@ -182,7 +182,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       tma_prefetch_2d(&maps.v, 64, ycoord(t));
     }
   };
-  if (tid == kTmaWarp * 32) {
+  if (warp == kTmaWarp && lane == 0) {
     for (int s2 = 0; s2 < 2; ++s2) {
       mbar_init(bar(BAR_K_FULL + s2), 1);
       mbar_init(bar(BAR_K_EMPTY + s2), 1);
@@ -195,10 +195,14 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
     mbar_init(bar(BAR_FINAL), 1);
     flags[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    tma_k(0, 0);
-    tma_v(0, 0);
-    if (ntiles > 1) tma_k(1, 1);
-    for (int t = 2; t < 2 + kPrefetch; ++t) prefetch(t);
+  }
+  if (warp == kTmaWarp) {
+    // the first K and V tiles from two threads at once (a thread issues about
+    // one box per ~570 cycles, and the set-up barrier waits for both); the
+    // second K tile and the L2 prefetches follow after the barrier
+    __syncwarp();
+    if (lane == 0) tma_k(0, 0);
+    else if (lane == 1) tma_v(0, 0);
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
@@ -252,7 +256,12 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
   // S^T_{t-2} freed its stage, V_t after O^T_{t-2} freed its stage.
   if (warp == kTmaWarp) {
     if (lane == 0) {
-      int nk = ntiles > 1 ? 2 : 1;
+      int nk = 1;
+      if (ntiles > 1) {
+        tma_k(1, 1);
+        nk = 2;
+      }
+      for (int t = 2; t < 2 + kPrefetch; ++t) prefetch(t);
       for (int t = 2; t < ntiles && !flags[1]; ++t) {
         if (!mbar_wait(bar(BAR_K_EMPTY + (t & 1)), ((t - 2) >> 1) & 1)) { flags[1] = 1; break; }
         tma_k(t, t & 1);
@@ -535,18 +544,25 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       }
       wg_bar(wg);
       const int d = key;  // O^T lane = output dim
+      // GRP chunks of O^T per TMEM wait, then their stores
 #pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        float v[4];
-        tmem_ld4(tm_o + lane_off + (uint32_t)(c0 + 4 * j), v);
+      for (int j0 = 0; j0 < NCH; j0 += GRP) {
+        float v[GRP][4];
+#pragma unroll
+        for (int u = 0; u < GRP; ++u)
+          if (j0 + u < NCH) tmem_ld4(tm_o + lane_off + (uint32_t)(c0 + 4 * (j0 + u)), v[u]);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int col = c0 + 4 * j + i;
-          if (col >= rows_here) break;
-          const float res = v[i] * alpha[col];
-          if (a.nsplit == 1) ((__nv_bfloat16*)a.out)[ooff[col] + d] = __float2bfloat16_rn(res);
-          else a.ws_o[ooff[col] + d] = res;
+        for (int u = 0; u < GRP; ++u) {
+          if (j0 + u >= NCH) break;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int col = c0 + 4 * (j0 + u) + i;
+            if (col >= rows_here) break;
+            const float res = v[u][i] * alpha[col];
+            if (a.nsplit == 1) ((__nv_bfloat16*)a.out)[ooff[col] + d] = __float2bfloat16_rn(res);
+            else a.ws_o[ooff[col] + d] = res;
+          }
         }
       }
     }
