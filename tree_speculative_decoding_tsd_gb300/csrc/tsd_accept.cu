@@ -159,7 +159,7 @@ extern "C" tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, 
   const ScanGeom g = scan_geometry(rows, V, 1, true);
   uint64_t* part = (uint64_t*)ws;
   launch(vocab_scan_kernel<true>, dim3((unsigned)(rows * g.nchunk)), dim3(kScanThreads), 0, st,
-      logits, V, 1, g.nchunk, g.chunk_len, part);
+      logits, V, 1, g.nchunk, g.chunk_len, part, g.one_wave);
   launch(accept_walk_kernel, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk, token,
       parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err);
   return cuda_status();
@@ -229,7 +229,7 @@ extern "C" tsd_status tsd_accept_walk_static(const float* logits, int B, int D, 
   const long rows = (long)B * R;
   const ScanGeom g = scan_geometry(rows, V, 1, true);
   launch(vocab_scan_kernel<true>, dim3((unsigned)(rows * g.nchunk)), dim3(kScanThreads), 0, st,
-      logits, V, 1, g.nchunk, g.chunk_len, part);
+      logits, V, 1, g.nchunk, g.chunk_len, part, g.one_wave);
   launch(accept_walk_kernel, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk, token,
       parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err);
   return cuda_status();

@@ -47,6 +47,20 @@ __device__ __forceinline__ void grid_dependency_sync() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
+// L2 prefetch of [p, p + bytes) by the bulk-copy unit, narrowed to whole
+// 16-byte units and to its first MiB.  A hint: nothing is returned and L2 stays coherent, so it
+// may precede grid_dependency_sync (a kernel launched early warms L2 with its
+// inputs while the previous kernel finishes).
+__device__ __forceinline__ void prefetch_l2(const void* p, long bytes) {
+  uintptr_t a = (uintptr_t)p, e = a + (uintptr_t)bytes;
+  a = (a + 15) & ~(uintptr_t)15;
+  e &= ~(uintptr_t)15;
+  if (e > a + (1u << 20)) e = a + (1u << 20);   // at most 1 MiB per hint
+  if (e > a)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(a), "r"((uint32_t)(e - a))
+                 : "memory");
+}
+
 // First device error wins; request index in the low 24 bits.
 __device__ __forceinline__ void report_error(int32_t* err, int code, int b) {
   if (err != nullptr) atomicCAS(err, 0, code | (b & 0xffffff));

@@ -37,6 +37,7 @@ constexpr int kScanMaxCand = 256;
 struct ScanGeom {
   int nchunk;
   int chunk_len;  // multiple of 256 elements
+  int one_wave;   // every CTA of the grid is resident at once
 };
 
 // Chunks per row: the count that minimises (waves of CTAs) x (chunk length +
@@ -61,6 +62,7 @@ inline ScanGeom scan_geometry(long rows, int V, int k, bool argmax) {
   ScanGeom g;
   g.chunk_len = (int)len;
   g.nchunk = (int)((V + len - 1) / len);
+  g.one_wave = rows * g.nchunk <= slots ? 1 : 0;
   return g;
 }
 
@@ -69,8 +71,7 @@ __device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p);
 template <bool kArgmax>
 __global__ void __launch_bounds__(kScanThreads, kArgmax ? kScanArgmaxPerSm : kScanTopkPerSm)
 vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chunk_len,
-                  uint64_t* __restrict__ out) {
-  grid_dependency_sync();
+                  uint64_t* __restrict__ out, int prefetch) {
   __shared__ uint64_t s_list[kScanWarps][32];
   __shared__ float s_max[kScanThreads];
   __shared__ float s_cut;
@@ -82,6 +83,10 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
   const int c1 = min(V, c0 + chunk_len);
   const float* xr = x + row * (long)V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // a grid of one wave is resident while the previous kernel finishes: its
+  // chunk is brought into L2 meanwhile (later waves would only add traffic)
+  if (prefetch && tid == 0) prefetch_l2(xr + c0, (long)(c1 - c0) * 4);
+  grid_dependency_sync();
 
   // Elements [c0, a0) and [a1, c1) are read one by one; [a0, a1) as float4.
   // x itself is 16-byte aligned, so alignment depends on row * V + index.

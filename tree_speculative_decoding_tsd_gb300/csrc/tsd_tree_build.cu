@@ -325,7 +325,7 @@ tsd_status tree_build_impl(const float* probs, int B, int S, int V, int k, int D
   const long ctas = (long)B * S * g.nchunk;
   uint64_t* part = (uint64_t*)ws;
   launch(vocab_scan_kernel<false>, dim3((unsigned)ctas), dim3(kScanThreads), 0, st, probs, V, k,
-      g.nchunk, g.chunk_len, part);
+      g.nchunk, g.chunk_len, part, g.one_wave);
   const auto tree_kernel = D + 2 <= 32   ? best_first_tree_kernel<1>
                            : D + 2 <= 64 ? best_first_tree_kernel<2>
                                          : best_first_tree_kernel<3>;

@@ -102,6 +102,34 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
     tma_desc_prefetch(&maps.kt);
     tma_desc_prefetch(&maps.vt);
   }
+  // While the previous kernel finishes: L2 prefetch of this CTA's first two
+  // prefix tiles (K and V, one warp each; contiguous cache only, the page
+  // table may still be being written) and of its Q rows.  Hints only.
+  {
+    const int w = threadIdx.x >> 5, ln = threadIdx.x & 31;
+    const int hk0 = blockIdx.y / a.nrg, b0 = blockIdx.z;
+    const int kp0 = blockIdx.x * a.split_len;
+    if (!kPaged && w < 4 && ln == 0) {
+      const int t = w >> 1;
+      const CUtensorMap* m = (w & 1) ? &maps.v : &maps.k;
+      if (kp0 + t * kKeys < a.cap) {
+        const int y = (b0 * a.Hkv + hk0) * a.cap + kp0 + t * kKeys;
+        tma_prefetch_2d(m, 0, y);
+        tma_prefetch_2d(m, 64, y);
+      }
+    } else if (w == 4) {
+      // packed rows [p0, p1) of this row group: for each tree row, the heads
+      // of this KV head are one contiguous run of q
+      const int p0 = (blockIdx.y % a.nrg) * rows_per_cta;
+      const int p1 = min(p0 + rows_per_cta, a.M);
+      for (int tr = p0 / a.g + ln; tr <= (p1 - 1) / a.g; tr += 32) {
+        const int h0 = max(p0, tr * a.g) - tr * a.g, h1 = min(p1, (tr + 1) * a.g) - tr * a.g;
+        const __nv_bfloat16* qr =
+            (const __nv_bfloat16*)a.q + (((long)b0 * a.R + tr) * a.Hq + hk0 * a.g + h0) * kD;
+        prefetch_l2(qr, (long)(h1 - h0) * kD * 2);
+      }
+    }
+  }
   grid_dependency_sync();
   constexpr int NH = L::NH;
   // 128-byte-swizzled TMA boxes and MMA operands need 1024-byte-aligned atoms:
