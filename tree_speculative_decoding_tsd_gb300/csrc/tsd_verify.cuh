@@ -99,6 +99,27 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// acc += w_(j+u) * O_(j+u) for u < m (m <= U, in increasing u), lane-strided
+// partials of DV = 32 * NV values at src[(j + u) * DV + 32 * t]; the weights
+// sit on lanes j..j+m-1 of wl.  All loads are issued before the products.
+template <int U, int NV>
+__device__ __forceinline__ void merge_batch(float (&acc)[NV], const float* src, float wl, int j,
+                                            int m) {
+  float x[U][NV];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+#pragma unroll
+    for (int t = 0; t < NV; ++t) x[u][t] = u < m ? src[(j + u) * NV * 32 + 32 * t] : 0.f;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const float w = __shfl_sync(kFull, wl, (j + u) & 31);
+    if (u < m) {
+#pragma unroll
+      for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, x[u][t], acc[t]);
+    }
+  }
+}
+
 // Merge the nsb split partials of one output row (b, r, h) with one warp.
 // Each split s left a normalised output O_s and its log2-sum-exp L_s; the
 // result is sum_s 2^(L_s - L) O_s with L = log2 sum_s 2^(L_s).
@@ -107,42 +128,33 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, int b, int r, 
                                              int lane) {
   const long row = ((long)b * a.R + r) * a.Hq + h;
   const long base = (((long)b * a.Hq + h) * a.R + r) * a.nsplit;
-  float mx = -INFINITY;
-  for (int s = lane; s < nsb; s += 32) mx = fmaxf(mx, a.ws_lse[base + s]);
+  // L = log2 sum_s 2^(L_s): maximum, then per-lane partial sums (split s on
+  // lane s % 32, in increasing s) reduced across the warp
+  const float l0 = lane < nsb ? a.ws_lse[base + lane] : -INFINITY;
+  float mx = l0;
+  for (int s = lane + 32; s < nsb; s += 32) mx = fmaxf(mx, a.ws_lse[base + s]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-  float sum = 0.f;
-  for (int s = lane; s < nsb; s += 32) sum += exp2f(a.ws_lse[base + s] - mx);
+  float sum = lane < nsb ? exp2f(l0 - mx) : 0.f;
+  for (int s = lane + 32; s < nsb; s += 32) sum += exp2f(a.ws_lse[base + s] - mx);
   sum = warp_sum(sum);
   const float tot = mx + log2f(sum);
   constexpr int NV = DV / 32;
-  constexpr int kU = DV <= 128 ? 8 : 4;  // partials in flight per lane: NV * kU loads
   float acc[NV];
 #pragma unroll
   for (int t = 0; t < NV; ++t) acc[t] = 0.f;
   // acc = sum over s in increasing order of fma(w_s, O_s, acc); lane j of a
-  // round of 32 splits holds w_(s0+j)
+  // round of 32 splits holds w_(s0+j).  Batches of kB partials have their
+  // loads in flight together; the rest is one predicated batch of kB or kB/2
+  constexpr int kB = NV > 4 ? 4 : 8;
   for (int s0 = 0; s0 < nsb; s0 += 32) {
     const int n = min(32, nsb - s0);
-    const float wl = lane < n ? exp2f(a.ws_lse[base + s0 + lane] - tot) : 0.f;
+    const float wl = lane >= n ? 0.f : exp2f((s0 == 0 ? l0 : a.ws_lse[base + s0 + lane]) - tot);
     const float* src = a.ws_o + (base + s0) * DV + lane;
-    // batches of kU partials; the loads past n are predicated off, so a row
-    // with at most kU splits (per round) takes one trip to L2
-    for (int j = 0; j < n; j += kU) {
-      float x[kU][NV];
-#pragma unroll
-      for (int u = 0; u < kU; ++u)
-#pragma unroll
-        for (int t = 0; t < NV; ++t) x[u][t] = j + u < n ? src[(j + u) * DV + 32 * t] : 0.f;
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const float w = __shfl_sync(kFull, wl, (j + u) & 31);
-        if (j + u < n) {
-#pragma unroll
-          for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, x[u][t], acc[t]);
-        }
-      }
-    }
+    int j = 0;
+    for (; j + kB <= n; j += kB) merge_batch<kB, NV>(acc, src, wl, j, kB);
+    if (n - j > kB / 2) merge_batch<kB, NV>(acc, src, wl, j, n - j);
+    else if (n - j > 0) merge_batch<kB / 2, NV>(acc, src, wl, j, n - j);
   }
 #pragma unroll
   for (int t = 0; t < NV; ++t) ((T*)a.out)[row * DV + lane + 32 * t] = cvt_out<T>(acc[t]);
