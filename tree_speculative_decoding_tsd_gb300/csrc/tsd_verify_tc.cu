@@ -417,9 +417,10 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
         masked(v, j);
       };
 
-      // optimistic pass with the current running max
+      // optimistic pass with the current running max (not on the first tile,
+      // which always takes the exact path below: nothing to take back out)
       float xmax = -INFINITY;
-      if (ok) {
+      if (ok && t > 0) {
 #pragma unroll
         for (int j0 = 0; j0 < NCH; j0 += GRP) {
           float v[GRP][4];
@@ -466,13 +467,15 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
         }
         wg_bar(wg);
         // take the optimistic probabilities back out (recomputed bit-identically)
+        if (t > 0) {
 #pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-          float v[4];
-          load1(v, j);
-          probs(v, j);
+          for (int j = 0; j < NCH; ++j) {
+            float v[4];
+            load1(v, j);
+            probs(v, j);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) l[4 * j + i] -= v[i];
+            for (int i = 0; i < 4; ++i) l[4 * j + i] -= v[i];
+          }
         }
         wg_bar(wg);
         for (int n = tid & 127; n < NH; n += 128) {
