@@ -132,6 +132,26 @@ def test_workspace_sizes_are_deterministic_and_scale():
     assert T.tsd_tree_build_workspace_size(0, 7, 100, 8) == 0
 
 
+# (rows, V, chunks per row) of the vocabulary scans, read back from the
+# workspace sizes (one k-candidate list per chunk).  Chunks minimise
+# (waves of resident CTAs) x (chunk length + a fixed per-chunk cost) on 152
+# SMs (4 top-k or 8 argmax CTAs each), and a row's lists hold at most 256
+# candidates: e.g. 7 top-k rows take 32 chunks of k=8 (one wave of 224 CTAs),
+# 224 rows take 5 (1120 CTAs, two waves of 608), 64 rows with k=10 take 9
+# (576 CTAs, one wave), 17 argmax rows take 66.
+@pytest.mark.parametrize("B,S,V,k,nchunk", [(1, 7, 151936, 8, 32), (32, 7, 151936, 8, 5),
+                                            (8, 8, 151936, 10, 9), (1, 3, 32, 2, 1)])
+def test_topk_scan_geometry(B, S, V, k, nchunk):
+    ws = T.tsd_tree_build_workspace_size(B, S, V, k)
+    assert ws == B * S * nchunk * k * 8
+    assert nchunk * k <= 256
+
+
+@pytest.mark.parametrize("B,D,V,nchunk", [(1, 16, 151936, 66), (32, 32, 151936, 8)])
+def test_argmax_scan_geometry(B, D, V, nchunk):
+    assert T.tsd_accept_walk_workspace_size(B, D, V) == B * (D + 1) * nchunk * 8
+
+
 @pytest.mark.parametrize("args", [dict(page_size=64), dict(page_size=100), dict(max_pages=3),
                                   dict(table=N), dict(table=U), dict(num_pages=0)])
 def test_paged_calls_reject(args):
