@@ -255,6 +255,18 @@ def test_verify_determinism_and_batch_consistency():
     assert (one.lse[0] - full.lse[b]).abs().max().item() <= 1e-3
 
 
+@pytest.mark.parametrize("dtype,Hq", [("bf16", 4), ("f32", 1)])
+def test_verify_many_splits_per_request(dtype, Hq):
+    """One request on one KV head with a 16000-key prefix: every row's result
+    is merged from 63 prefix splits (several batches of partials and two
+    rounds of 32 split weights in the merge), on the tcgen05 path (bf16, four
+    query heads: 20 packed rows) and the CUDA-core path (fp32)."""
+    over = dict(B=1, D=4, Hq=Hq, Hkv=1, P=16000, P_min=16000, V=500, dtype=dtype)
+    d = inputs("qwen", **over)
+    w = d["w"]
+    check_attention(w, *attn_inputs(w), d["tree"]["mask"])
+
+
 # ---------------------------------------------------------- accept walk --
 
 def run_walk(step, logits):
