@@ -449,6 +449,54 @@ def test_full_step_chained(name, over):
     assert int(step.err[0]) == 0
 
 
+def test_rounds_enqueued_back_to_back():
+    """Three full rounds enqueued on one stream with no host synchronisation
+    in between (each round's first kernel may be scheduled while the previous
+    round's commit finishes): the final cache and prefix lengths equal three
+    oracle rounds applied in order, and the last round's tree, attention
+    (over the cache the first two rounds extended) and walk match."""
+    w = W.WORKLOADS["qwen"].scaled(B=3, V=5000, P=300, P_min=100)
+    base_lg = W.draft_logits(w)
+    root = W.root_tokens(w)
+    q, kc, vc, _, kt, vt = attn_inputs(w)
+    plen = torch.tensor([50, 120, 0], dtype=torch.int32)   # room for three rounds
+    kc_ref, vc_ref, pl_ref = W.bits(kc).copy(), W.bits(vc).copy(), plen.numpy().copy()
+    rounds = []
+    for r in range(3):
+        lg = torch.roll(base_lg, shifts=101 * r, dims=-1)
+        probs = W.draft_probs(w, lg)
+        tp, ti = oracle.topk(probs.numpy(), w.k)
+        tree = oracle.tree(tp, ti, w.D, root.numpy(), method="beam")
+        tl = W.target_logits(w, torch.from_numpy(tree["depth"]), lg)
+        ktr, vtr = torch.roll(kt, shifts=r, dims=1), torch.roll(vt, shifts=r, dims=1)
+        walk = oracle.accept_walk(oracle.argmax(tl.numpy()), tree, w.S)
+        if r == 2:
+            sel = sample_rows(w, 24, seed=9)
+            ref_out, _ = oracle.verify_attn(W.bits(q), kc_ref, vc_ref, pl_ref.copy(), W.bits(ktr),
+                                            W.bits(vtr), tree["mask"], w.scale, sel=sel)
+        oracle.commit(W.bits(ktr), W.bits(vtr), walk["accept_rows"], walk["accept_len"], kc_ref,
+                      vc_ref, pl_ref, w.S)
+        rounds.append((probs, tl, ktr, vtr, tree, walk))
+    step = TreeVerifyStep.for_workload(w, DEV)
+    gq, gkc, gvc, gpl, groot = gpu(q, kc, vc, plen, root)
+    dev_rounds = [gpu(p_, tl_, kt_, vt_) for p_, tl_, kt_, vt_, _, _ in rounds]
+    torch.cuda.synchronize()
+    for gp, gtl, gkt, gvt in dev_rounds:
+        step.run(gp, groot, gq, gkc, gvc, gpl, gkt, gvt, gtl)
+    torch.cuda.synchronize()
+    assert int(step.err[0]) == 0
+    np.testing.assert_array_equal(W.bits(gkc.cpu()), kc_ref)
+    np.testing.assert_array_equal(W.bits(gvc.cpu()), vc_ref)
+    np.testing.assert_array_equal(gpl.cpu().numpy(), pl_ref)
+    tree, walk = rounds[2][4], rounds[2][5]
+    np.testing.assert_array_equal(step.tree.token.cpu().numpy(), tree["token"])
+    np.testing.assert_array_equal(step.tree.mask.cpu().numpy().view(np.uint64), tree["mask"])
+    out = step.out.float().cpu().numpy()
+    assert np.abs(np.stack([out[b, r, h] for b, r, h in sel]) - ref_out).max() <= _tol(w)
+    for key in ("accept_len", "accept_rows", "bonus", "chain_id"):
+        np.testing.assert_array_equal(getattr(step.walk, key).cpu().numpy(), walk[key])
+
+
 # ------------------------------------------------- every attention path --
 
 @pytest.fixture
