@@ -685,11 +685,22 @@ def cpu_baseline(w, host, seconds, min_steps=1):
             if steps >= min_steps:
                 break
     t = (time.perf_counter() - t0) / steps
+    # the same step on one thread (one step at least, about a third of the budget)
+    t1_0 = time.perf_counter()
+    steps1 = 0
+    while True:
+        oracle_step(w, host, [0], nthreads=1)
+        steps1 += 1
+        if time.perf_counter() - t1_0 >= seconds / 3 or steps1 >= 1000:
+            break
+    t1 = (time.perf_counter() - t1_0) / steps1
     return {"value": round(n_req * w.D / t, 3), "unit": "nodes/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{steps} full oracle step(s) of request 0 of the {w.name} workload "
                       f"({w.D} nodes each; all {w.R * w.Hq} attention rows in fp64), "
-                      f"{t:.3f} s per step"}
+                      f"{t:.3f} s per step",
+            "s_per_step_all_cores": round(t, 4),
+            "s_per_step_one_thread": round(t1, 4)}
 
 
 def run_reference(args, dist):
