@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
+from tree_speculative_decoding_tsd_gb300 import workloads as W
 from tests.conftest import load_golden
 
 RNG = np.random.default_rng(1234)
@@ -157,6 +158,21 @@ def test_tree_enum_equals_beam(S, k, D, quant):
     _, tp, ti, root = _random_tree(4, S, k, D, quantize=quant)
     a = oracle.tree(tp, ti, D, root, "enum")
     b = oracle.tree(tp, ti, D, root, "beam")
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+
+
+@pytest.mark.parametrize("name,B", [("toy", None), ("qwen", None), ("batched", 4), ("mla", None)])
+def test_tree_enum_equals_beam_on_workload_inputs(name, B):
+    """The level beam (used where enumeration is out of reach) gives the same
+    tree bytes as enumerating every path, on the workloads' own marginals
+    (at most 8^7 paths per request)."""
+    w = W.WORKLOADS[name] if B is None else W.WORKLOADS[name].scaled(B=B)
+    probs = W.draft_probs(w, W.draft_logits(w))
+    tp, ti = oracle.topk(probs.numpy(), w.k)
+    root = W.root_tokens(w).numpy()
+    a = oracle.tree(tp, ti, w.D, root, "enum")
+    b = oracle.tree(tp, ti, w.D, root, "beam")
     for key in a:
         np.testing.assert_array_equal(a[key], b[key], err_msg=key)
 
