@@ -32,7 +32,11 @@
  *     caller-provided workspace of the size the matching *_workspace_size call
  *     returns (for the current device).
  *   - Every call only enqueues kernels on `stream` and returns.  Outputs are
- *     valid once the stream has reached that point.
+ *     valid once the stream has reached that point.  Kernels are launched
+ *     with programmatic stream serialisation: one may be scheduled while the
+ *     kernel before it on the stream is finishing, but it reads and writes
+ *     no memory before that kernel has completed, so stream order is kept
+ *     (its set-up and L2 prefetch hints overlap the predecessor).
  *   - The return value reports HOST-side validation and launch errors.  On any
  *     non-OK return nothing was enqueued, except TSD_ERR_CUDA from a failed
  *     launch (check cudaGetLastError semantics).
