@@ -234,6 +234,25 @@ tsd_status tsd_tree_verify_attn(const tsd_attn_desc* desc, const void* q,
                                 size_t ws_bytes, int32_t* err,
                                 tsd_stream_t stream);
 
+/* Attention paths of tsd_tree_verify_attn / tsd_tree_verify_attn_paged.  The
+ * automatic choice is tcgen05 for bf16 heads of 128 dims with at least 16
+ * packed rows (tree rows x query heads per KV head) and for latent heads with
+ * at least 64; the legacy mma.sync path for other bf16 heads of 64 or 128
+ * dims with at least 64 packed rows; CUDA cores (fp32 arithmetic) otherwise. */
+#define TSD_PATH_AUTO 0
+#define TSD_PATH_CUDA_CORE 1
+#define TSD_PATH_MMA_SYNC 2
+#define TSD_PATH_TCGEN05 3
+
+/* Diagnostic: force one attention path for the verify calls that follow, and
+ * for tsd_verify_workspace_size (a forced path that cannot run a given call
+ * falls back to the automatic choice).  No counterpart on the pages: it lets
+ * tests check every path against an independent reference.  The setting is
+ * process-wide; change it only while no other thread is enqueueing verify
+ * calls, and size workspaces under the same setting as the calls.  Returns
+ * the previous setting, or -1 (and changes nothing) for an unknown path. */
+int tsd_set_verify_path(int path);
+
 /* --------------------------------------------------------------------------
  * Paged KV cache: tsd_tree_verify_attn_paged, tsd_commit_path_paged
  *

@@ -501,14 +501,8 @@ def test_rounds_enqueued_back_to_back():
 
 @pytest.fixture
 def force_path(request):
-    import os
-    old = os.environ.get("TSD_VERIFY_PATH")
-    os.environ["TSD_VERIFY_PATH"] = request.param
-    yield request.param
-    if old is None:
-        os.environ.pop("TSD_VERIFY_PATH", None)
-    else:
-        os.environ["TSD_VERIFY_PATH"] = old
+    with T.verify_path(request.param):
+        yield request.param
 
 
 @pytest.mark.parametrize("force_path", ["tc", "mma", "generic"], indirect=True)
@@ -598,10 +592,14 @@ def test_verify_latent_rescale_on_late_large_scores(force_path):
 
 @pytest.mark.parametrize("name,force", [("qwen", "tc"), ("qwen", "mma"), ("qwen", "generic"),
                                         ("mla", "tc"), ("mla", "generic")])
-def test_verify_ignores_nonfinite_cache_rows_past_prefix(name, force, monkeypatch):
+def test_verify_ignores_nonfinite_cache_rows_past_prefix(name, force):
     """Cache rows at and past prefix_len hold NaN/Inf: tiles that straddle the
     end of the prefix must not let them reach the output (0 x NaN)."""
-    monkeypatch.setenv("TSD_VERIFY_PATH", force)
+    with T.verify_path(force):
+        _nonfinite_case(name)
+
+
+def _nonfinite_case(name):
     over = dict(B=3, P=700, P_min=100, V=1000)
     d = inputs(name, **over)
     w = d["w"]
@@ -874,11 +872,14 @@ def _gather(pool, table, page_size):
     ("mla", dict(B=2, P=700, P_min=300, V=2000), 128, "tc"),
     ("toy", dict(), 128, None),
 ])
-def test_paged_verify_equals_contiguous(name, over, page_size, force, monkeypatch):
+def test_paged_verify_equals_contiguous(name, over, page_size, force):
     """Verify through a shuffled page pool gives the same bytes as the
     contiguous cache, and matches the oracle on the gathered cache."""
-    if force:
-        monkeypatch.setenv("TSD_VERIFY_PATH", force)
+    with T.verify_path(force or "auto"):
+        _paged_case(name, over, page_size)
+
+
+def _paged_case(name, over, page_size):
     d = inputs(name, **over)
     w = d["w"]
     cap = -(-w.cap // page_size) * page_size
@@ -950,10 +951,8 @@ def test_paged_bad_page_is_reported_not_read():
     kpool, table = _paged(kc, page_size, seed=1)
     vpool = _paged(vc, page_size, seed=1)[0]
     table[1, 2] = kpool.shape[0] + 100     # request 1, positions 256..383: outside the pool
-    import os
     for force in ("tc", "generic"):
-        os.environ["TSD_VERIFY_PATH"] = force
-        try:
+        with T.verify_path(force):
             # the workspace follows the plan of the forced path
             step = TreeVerifyStep(w.B, w.S, w.V, w.k, w.D, w.Hq, w.Hkv, w.dk, w.dv, cap,
                                   w.torch_dtype, w.v_aliases_k, w.scale, DEV)
@@ -964,6 +963,4 @@ def test_paged_bad_page_is_reported_not_read():
                                          g[6], step.tree.mask, step.out, step.lse, step.ws_verify,
                                          step.err)
             torch.cuda.synchronize()
-        finally:
-            os.environ.pop("TSD_VERIFY_PATH", None)
         assert int(step.err[0]) == (T.TSD_DEV_ERR_BAD_PAGE | 1), force

@@ -1,10 +1,12 @@
 """Python binding of ``libtsd.so``, the GB300 tree-speculative-decoding verify step.
 
-Argument marshalling only: every function takes torch CUDA tensors, passes
-their device pointers to the C ABI declared in ``include/tsd.h`` (same names),
-and raises :class:`TsdError` on a non-OK status.  All arithmetic runs in the
-library's CUDA kernels; there is no CPU fallback -- importing this package
-fails if the compiled library is missing.
+Argument marshalling only: every function takes torch CUDA tensors, checks
+their element types and shapes, passes their device pointers to the C ABI
+declared in ``include/tsd.h`` (same names), and raises :class:`TsdError` on a
+non-OK status.  All arithmetic runs in the library's CUDA kernels; there is no
+CPU fallback.  The library is loaded on first use (``lib``), so importing the
+package, or its input generators in ``workloads``, maps nothing; the first
+call fails with ImportError if the compiled library is missing.
 
 Typical step on one stream::
 
@@ -40,6 +42,7 @@ TSD_DEV_ERR_TIMEOUT = 0x03000000
 TSD_DEV_ERR_MASK = 0x7F000000
 TSD_F32 = 0
 TSD_BF16 = 1
+VERIFY_PATHS = {"auto": 0, "generic": 1, "mma": 2, "tc": 3}   # TSD_PATH_* of tsd.h
 
 # every symbol the header declares
 EXPORTED = ("tsd_status_string", "tsd_version", "tsd_tree_build_workspace_size",
@@ -47,7 +50,7 @@ EXPORTED = ("tsd_status_string", "tsd_version", "tsd_tree_build_workspace_size",
             "tsd_verify_workspace_size",
             "tsd_tree_verify_attn", "tsd_tree_verify_attn_paged", "tsd_commit_path_paged",
             "tsd_accept_walk_workspace_size", "tsd_accept_walk", "tsd_accept_walk_static",
-            "tsd_commit_path")
+            "tsd_commit_path", "tsd_set_verify_path")
 
 
 class TsdError(RuntimeError):
@@ -99,18 +102,59 @@ def _load():
     lib.tsd_commit_path_paged.argtypes = [ctypes.POINTER(tsd_attn_desc), I, P, P, P, P, P, P, P, I,
                                           I, I, P, P, P]
     lib.tsd_commit_path_paged.restype = I
+    lib.tsd_set_verify_path.argtypes = [I]
+    lib.tsd_set_verify_path.restype = I
     return lib
 
 
-lib = _load()
+_lib = None
+
+
+def _L():
+    """The loaded library (loaded on first use; ImportError if it is not built)."""
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def __getattr__(name):
+    if name == "lib":
+        return _L()
+    raise AttributeError(f"module {__name__!r} has no attribute {name!r}")
+
+
+def tsd_set_verify_path(path) -> int:
+    """Force an attention path ("auto", "generic", "mma", "tc" or a TSD_PATH_*
+    value) for the verify calls that follow; returns the previous value."""
+    code = VERIFY_PATHS[path] if isinstance(path, str) else int(path)
+    prev = _L().tsd_set_verify_path(code)
+    if prev < 0:
+        raise ValueError(f"unknown verify path {path!r}")
+    return prev
+
+
+class verify_path:
+    """Context manager: the verify calls inside use the given path."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        self.prev = tsd_set_verify_path(self.path)
+        return self
+
+    def __exit__(self, *exc):
+        tsd_set_verify_path(self.prev)
+        return False
 
 
 def tsd_status_string(status: int) -> str:
-    return lib.tsd_status_string(int(status)).decode()
+    return _L().tsd_status_string(int(status)).decode()
 
 
 def tsd_version() -> int:
-    return lib.tsd_version()
+    return _L().tsd_version()
 
 
 def _ptr(t):
@@ -151,92 +195,177 @@ def workspace(nbytes: int, device=None) -> torch.Tensor:
 
 # ------------------------------------------------------------------ calls --
 
+_I32, _F32, _U8 = torch.int32, torch.float32, torch.uint8
+_MASK = (torch.int64,) + ((torch.uint64,) if hasattr(torch, "uint64") else ())
+
+
+def _t(t, name, dtypes, shape=None):
+    """Device pointer of ``t`` after checking its element type and shape
+    (None passes through as a NULL pointer)."""
+    if t is None:
+        return None
+    if not isinstance(dtypes, tuple):
+        dtypes = (dtypes,)
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: element type {t.dtype}, expected "
+                        f"{' or '.join(str(d) for d in dtypes)}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return _ptr(t)
+
+
+def _err(err):
+    return _t(err, "err", _I32)
+
+
+def _tree(B, R, token, parent, depth, score, mask, is_leaf):
+    return (_t(token, "token", _I32, (B, R)), _t(parent, "parent", _I32, (B, R)),
+            _t(depth, "depth", _I32, (B, R)), _t(score, "score", _F32, (B, R)),
+            _t(mask, "mask", _MASK, (B, R)), _t(is_leaf, "is_leaf", _U8, (B, R)))
+
+
+def _attn_dtype(desc):
+    return torch.bfloat16 if desc.dtype == TSD_BF16 else torch.float32
+
+
 def tsd_tree_build_workspace_size(B, S, V, k) -> int:
-    return lib.tsd_tree_build_workspace_size(B, S, V, k)
+    return _L().tsd_tree_build_workspace_size(B, S, V, k)
 
 
 def tsd_tree_build(probs, k, D, root_tok, token, parent, depth, score, mask, is_leaf, ws,
                    err=None, stream=None):
     B, S, V = probs.shape
-    _check("tsd_tree_build", lib.tsd_tree_build(
-        _ptr(probs), B, S, V, k, D, _ptr(root_tok), _ptr(token), _ptr(parent), _ptr(depth),
-        _ptr(score), _ptr(mask), _ptr(is_leaf), _ptr(ws), _nbytes(ws), _ptr(err),
-        _stream(stream)))
+    _check("tsd_tree_build", _L().tsd_tree_build(
+        _t(probs, "probs", _F32), B, S, V, k, D, _t(root_tok, "root_tok", _I32, (B,)),
+        *_tree(B, D + 1, token, parent, depth, score, mask, is_leaf), _ptr(ws), _nbytes(ws),
+        _err(err), _stream(stream)))
 
 
 def tsd_tree_build_adaptive(probs, k, D_max, root_tok, cost_d, cost_v, token, parent, depth,
                             score, mask, is_leaf, n_nodes, ws, err=None, stream=None):
     B, S, V = probs.shape
-    _check("tsd_tree_build_adaptive", lib.tsd_tree_build_adaptive(
-        _ptr(probs), B, S, V, k, D_max, _ptr(root_tok), _ptr(cost_d), _ptr(cost_v), _ptr(token),
-        _ptr(parent), _ptr(depth), _ptr(score), _ptr(mask), _ptr(is_leaf), _ptr(n_nodes),
-        _ptr(ws), _nbytes(ws), _ptr(err), _stream(stream)))
+    _check("tsd_tree_build_adaptive", _L().tsd_tree_build_adaptive(
+        _t(probs, "probs", _F32), B, S, V, k, D_max, _t(root_tok, "root_tok", _I32, (B,)),
+        _t(cost_d, "cost_d", _F32, (B,)), _t(cost_v, "cost_v", _F32, (B, D_max + 1)),
+        *_tree(B, D_max + 1, token, parent, depth, score, mask, is_leaf),
+        _t(n_nodes, "n_nodes", _I32, (B,)), _ptr(ws), _nbytes(ws), _err(err), _stream(stream)))
 
 
 def tsd_tree_build_conditioned(cand_p, cand_tok, cand_parent, D, root_tok, token, parent, depth,
                                score, mask, is_leaf, err=None, stream=None):
     B, C = cand_p.shape
-    _check("tsd_tree_build_conditioned", lib.tsd_tree_build_conditioned(
-        _ptr(cand_p), _ptr(cand_tok), _ptr(cand_parent), B, C, D, _ptr(root_tok), _ptr(token),
-        _ptr(parent), _ptr(depth), _ptr(score), _ptr(mask), _ptr(is_leaf), _ptr(err),
+    _check("tsd_tree_build_conditioned", _L().tsd_tree_build_conditioned(
+        _t(cand_p, "cand_p", _F32), _t(cand_tok, "cand_tok", _I32, (B, C)),
+        _t(cand_parent, "cand_parent", _I32, (B, C)), B, C, D,
+        _t(root_tok, "root_tok", _I32, (B,)),
+        *_tree(B, D + 1, token, parent, depth, score, mask, is_leaf), _err(err),
         _stream(stream)))
 
 
 def tsd_verify_workspace_size(desc: tsd_attn_desc) -> int:
-    return lib.tsd_verify_workspace_size(ctypes.byref(desc))
+    return _L().tsd_verify_workspace_size(ctypes.byref(desc))
+
+
+def _verify_common(desc, q, prefix_len, ktree, vtree, mask, out, lse):
+    d = desc
+    dt = _attn_dtype(d)
+    alias = bool(d.v_aliases_k)
+    return (_t(q, "q", dt, (d.B, d.R, d.Hq, d.dk)), _t(prefix_len, "prefix_len", _I32, (d.B,)),
+            _t(ktree, "ktree", dt, (d.B, d.R, d.Hkv, d.dk)),
+            None if alias else _t(vtree, "vtree", dt, (d.B, d.R, d.Hkv, d.dv)),
+            _t(mask, "mask", _MASK, (d.B, d.R)), _t(out, "out", dt, (d.B, d.R, d.Hq, d.dv)),
+            _t(lse, "lse", _F32, (d.B, d.R, d.Hq)))
 
 
 def tsd_tree_verify_attn(desc, q, kcache, vcache, prefix_len, ktree, vtree, mask, out, lse, ws,
                          err=None, stream=None):
-    _check("tsd_tree_verify_attn", lib.tsd_tree_verify_attn(
-        ctypes.byref(desc), _ptr(q), _ptr(kcache), _ptr(vcache), _ptr(prefix_len), _ptr(ktree),
-        _ptr(vtree), _ptr(mask), _ptr(out), _ptr(lse), _ptr(ws), _nbytes(ws), _ptr(err),
-        _stream(stream)))
+    d = desc
+    dt = _attn_dtype(d)
+    pq, pl, pkt, pvt, pm, po, pls = _verify_common(d, q, prefix_len, ktree, vtree, mask, out, lse)
+    pkc = _t(kcache, "kcache", dt, (d.B, d.Hkv, d.cap, d.dk))
+    pvc = None if d.v_aliases_k else _t(vcache, "vcache", dt, (d.B, d.Hkv, d.cap, d.dv))
+    _check("tsd_tree_verify_attn", _L().tsd_tree_verify_attn(
+        ctypes.byref(d), pq, pkc, pvc, pl, pkt, pvt, pm, po, pls, _ptr(ws), _nbytes(ws),
+        _err(err), _stream(stream)))
 
 
 def tsd_accept_walk_workspace_size(B, D, V) -> int:
-    return lib.tsd_accept_walk_workspace_size(B, D, V)
+    return _L().tsd_accept_walk_workspace_size(B, D, V)
+
+
+def _walk_args(logits, S, token, parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus,
+               chain_id):
+    B, R, V = logits.shape
+    return (_t(logits, "logits", _F32), B, R - 1, S, V, _t(token, "token", _I32, (B, R)),
+            _t(parent, "parent", _I32, (B, R)), _t(mask, "mask", _MASK, (B, R)),
+            _t(is_leaf, "is_leaf", _U8, (B, R)), _t(tgt, "tgt", _I32, (B, R)),
+            _t(accept_len, "accept_len", _I32, (B,)),
+            _t(accept_rows, "accept_rows", _I32, (B, S + 1)), _t(bonus, "bonus", _I32, (B,)),
+            _t(chain_id, "chain_id", _I32, (B,)))
 
 
 def tsd_accept_walk(logits, S, token, parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus,
                     chain_id, ws, err=None, stream=None):
-    B, R, V = logits.shape
-    _check("tsd_accept_walk", lib.tsd_accept_walk(
-        _ptr(logits), B, R - 1, S, V, _ptr(token), _ptr(parent), _ptr(mask), _ptr(is_leaf),
-        _ptr(tgt), _ptr(accept_len), _ptr(accept_rows), _ptr(bonus), _ptr(chain_id), _ptr(ws),
-        _nbytes(ws), _ptr(err), _stream(stream)))
+    _check("tsd_accept_walk", _L().tsd_accept_walk(
+        *_walk_args(logits, S, token, parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus,
+                    chain_id), _ptr(ws), _nbytes(ws), _err(err), _stream(stream)))
 
 
 def tsd_accept_walk_static(logits, S, token, parent, mask, is_leaf, tgt, accept_len, accept_rows,
                            bonus, chain_id, err=None, stream=None):
     """tsd_accept_walk without a workspace (fixed in-library scratch; see tsd.h)."""
-    B, R, V = logits.shape
-    _check("tsd_accept_walk_static", lib.tsd_accept_walk_static(
-        _ptr(logits), B, R - 1, S, V, _ptr(token), _ptr(parent), _ptr(mask), _ptr(is_leaf),
-        _ptr(tgt), _ptr(accept_len), _ptr(accept_rows), _ptr(bonus), _ptr(chain_id), _ptr(err),
-        _stream(stream)))
+    _check("tsd_accept_walk_static", _L().tsd_accept_walk_static(
+        *_walk_args(logits, S, token, parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus,
+                    chain_id), _err(err), _stream(stream)))
 
 
 def tsd_tree_verify_attn_paged(desc, q, kpool, vpool, page_table, page_size, prefix_len, ktree,
                                vtree, mask, out, lse, ws, err=None, stream=None):
     """page_table [B][max_pages] int32; pools [num_pages][Hkv][page_size][d]."""
-    _check("tsd_tree_verify_attn_paged", lib.tsd_tree_verify_attn_paged(
-        ctypes.byref(desc), _ptr(q), _ptr(kpool), _ptr(vpool), _ptr(page_table),
-        page_table.shape[1], page_size, kpool.shape[0], _ptr(prefix_len), _ptr(ktree),
-        _ptr(vtree), _ptr(mask), _ptr(out), _ptr(lse), _ptr(ws), _nbytes(ws), _ptr(err),
+    d = desc
+    dt = _attn_dtype(d)
+    pq, pl, pkt, pvt, pm, po, pls = _verify_common(d, q, prefix_len, ktree, vtree, mask, out, lse)
+    npg, mp = kpool.shape[0], page_table.shape[1]
+    pkp = _t(kpool, "kpool", dt, (npg, d.Hkv, page_size, d.dk))
+    pvp = None if d.v_aliases_k else _t(vpool, "vpool", dt, (npg, d.Hkv, page_size, d.dv))
+    _check("tsd_tree_verify_attn_paged", _L().tsd_tree_verify_attn_paged(
+        ctypes.byref(d), pq, pkp, pvp, _t(page_table, "page_table", _I32, (d.B, mp)), mp,
+        page_size, npg, pl, pkt, pvt, pm, po, pls, _ptr(ws), _nbytes(ws), _err(err),
         _stream(stream)))
+
+
+def _commit_common(desc, S, ktree, vtree, accept_rows, accept_len, prefix_len):
+    d = desc
+    dt = _attn_dtype(d)
+    return (_t(ktree, "ktree", dt, (d.B, d.R, d.Hkv, d.dk)),
+            None if d.v_aliases_k else _t(vtree, "vtree", dt, (d.B, d.R, d.Hkv, d.dv)),
+            _t(accept_rows, "accept_rows", _I32, (d.B, S + 1)),
+            _t(accept_len, "accept_len", _I32, (d.B,)),
+            _t(prefix_len, "prefix_len", _I32, (d.B,)))
 
 
 def tsd_commit_path_paged(desc, S, ktree, vtree, accept_rows, accept_len, kpool, vpool,
                           page_table, page_size, prefix_len, err=None, stream=None):
-    _check("tsd_commit_path_paged", lib.tsd_commit_path_paged(
-        ctypes.byref(desc), S, _ptr(ktree), _ptr(vtree), _ptr(accept_rows), _ptr(accept_len),
-        _ptr(kpool), _ptr(vpool), _ptr(page_table), page_table.shape[1], page_size,
-        kpool.shape[0], _ptr(prefix_len), _ptr(err), _stream(stream)))
+    d = desc
+    dt = _attn_dtype(d)
+    pkt, pvt, par, pal, ppl = _commit_common(d, S, ktree, vtree, accept_rows, accept_len,
+                                             prefix_len)
+    npg, mp = kpool.shape[0], page_table.shape[1]
+    pkp = _t(kpool, "kpool", dt, (npg, d.Hkv, page_size, d.dk))
+    pvp = None if d.v_aliases_k else _t(vpool, "vpool", dt, (npg, d.Hkv, page_size, d.dv))
+    _check("tsd_commit_path_paged", _L().tsd_commit_path_paged(
+        ctypes.byref(d), S, pkt, pvt, par, pal, pkp, pvp,
+        _t(page_table, "page_table", _I32, (d.B, mp)), mp, page_size, npg, ppl, _err(err),
+        _stream(stream)))
 
 
 def tsd_commit_path(desc, S, ktree, vtree, accept_rows, accept_len, kcache, vcache, prefix_len,
                     err=None, stream=None):
-    _check("tsd_commit_path", lib.tsd_commit_path(
-        ctypes.byref(desc), S, _ptr(ktree), _ptr(vtree), _ptr(accept_rows), _ptr(accept_len),
-        _ptr(kcache), _ptr(vcache), _ptr(prefix_len), _ptr(err), _stream(stream)))
+    d = desc
+    dt = _attn_dtype(d)
+    pkt, pvt, par, pal, ppl = _commit_common(d, S, ktree, vtree, accept_rows, accept_len,
+                                             prefix_len)
+    pkc = _t(kcache, "kcache", dt, (d.B, d.Hkv, d.cap, d.dk))
+    pvc = None if d.v_aliases_k else _t(vcache, "vcache", dt, (d.B, d.Hkv, d.cap, d.dv))
+    _check("tsd_commit_path", _L().tsd_commit_path(
+        ctypes.byref(d), S, pkt, pvt, par, pal, pkc, pvc, ppl, _err(err), _stream(stream)))

@@ -31,6 +31,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "tsd_common.cuh"
@@ -172,8 +174,11 @@ verify_generic_kernel(const __grid_constant__ VerifyArgs a) {
 
 // ---------------------------------------------------------------- planning --
 
-// Path choice.  TSD_VERIFY_PATH=generic|mma|tc forces a path where it
-// applies (used by the tests to check every path against the oracle).
+// Path choice.  tsd_set_verify_path forces a path where it applies (the
+// tests use it to check every path against the oracle); the default is the
+// automatic choice below.
+static std::atomic<int> g_forced_path{TSD_PATH_AUTO};
+
 static int choose_path(const tsd_attn_desc& d, int M) {
   const bool gqa_bf16 = d.dtype == TSD_BF16 && !d.v_aliases_k && d.dk == d.dv;
   const bool mma_ok = gqa_bf16 && (d.dk == 64 || d.dk == 128);
@@ -181,11 +186,11 @@ static int choose_path(const tsd_attn_desc& d, int M) {
   // tcgen05 with the packed rows on the MMA N dimension works from N = 16 up
   const bool tc_ok = ((gqa_bf16 && d.dk == 128 && M >= kTcMinRows) ||
                       (mla_bf16 && M >= kMmaMinRows)) && tc_path_available();
-  const char* force = getenv("TSD_VERIFY_PATH");
-  if (force != nullptr) {
-    if (strcmp(force, "generic") == 0) return kPathGeneric;
-    if (strcmp(force, "mma") == 0 && mma_ok) return kPathMma;
-    if (strcmp(force, "tc") == 0 && tc_ok) return kPathTc;
+  switch (g_forced_path.load(std::memory_order_relaxed)) {
+    case TSD_PATH_CUDA_CORE: return kPathGeneric;
+    case TSD_PATH_MMA_SYNC: if (mma_ok) return kPathMma; break;
+    case TSD_PATH_TCGEN05: if (tc_ok) return kPathTc; break;
+    default: break;
   }
   if (tc_ok) return kPathTc;
   if (M < kMmaMinRows) return kPathGeneric;  // not a dense contraction
@@ -298,6 +303,11 @@ static bool desc_ok(const tsd_attn_desc* d) {
   const bool mla = d->v_aliases_k && d->dk == 576 && d->dv == 512;
   const bool gqa = !d->v_aliases_k && d->dk == d->dv && (d->dk == 64 || d->dk == 128);
   return mla || gqa;
+}
+
+extern "C" int tsd_set_verify_path(int path) {
+  if (path < TSD_PATH_AUTO || path > TSD_PATH_TCGEN05) return -1;
+  return g_forced_path.exchange(path);
 }
 
 extern "C" size_t tsd_verify_workspace_size(const tsd_attn_desc* d) {
