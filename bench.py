@@ -5,9 +5,12 @@ tree) -> tsd_tree_verify_attn (branch-aware attention) -> tsd_accept_walk
 (argmax + greedy walk) -> tsd_commit_path (accepted-path KV commit), chained
 on one stream.  Metric: verified tree nodes per second (B * D per step).
 
-Default workload: the Qwen3-8B-like GQA verify (B=1, 32 q / 8 KV heads, head
-dim 128, bf16 KV, prefix 2048, vocab 151936, depth 7, top-8, budget 16).
-Other workloads: --config toy|qwen|batched|long|mla.
+Default workload: the long-context GQA verify (B=8, 32 q / 8 KV heads, head
+dim 128, bf16 KV, prefix 32768, vocab 151936, depth 8, top-10, budget 64), the
+largest single-GPU configuration and one of the two the HBM-roofline target is
+stated on; the same line also carries the other one, the batched serving
+workload (B=32, prefixes U{1024..4096}, budget 32), measured the same way
+(--also, "" to skip).  Other workloads: --config toy|qwen|batched|long|mla.
 
 Timing: W untimed warm-up steps, then K steps, each replayed from a CUDA
 graph of the four calls and bracketed by CUDA events on the launching
@@ -57,7 +60,10 @@ def parse():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--config", default="qwen", choices=list(W.WORKLOADS))
+    p.add_argument("--config", default="long", choices=list(W.WORKLOADS))
+    p.add_argument("--also", default="batched",
+                   help="comma-separated workloads measured in the same run (step and "
+                        "per-call times, roofline), reported under 'also'")
     p.add_argument("--no-graph", action="store_true", help="time eager calls, not graph replay")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="budget of the CPU-oracle baseline sample")
@@ -314,13 +320,16 @@ CALL_SOURCES = {
 
 # ---------------------------------------------------------------- ours ----
 
-def run_ours(args, dist):
+def run_ours(args, dist, config=None, lite=False):
+    """Measure one workload.  lite: the whole step and the per-call times only
+    (no end-to-end, adaptive or paged legs)."""
     import tree_speculative_decoding_tsd_gb300 as T
     from tree_speculative_decoding_tsd_gb300.step import TreeVerifyStep
 
+    config = config or args.config
     dev = torch.device("cuda", dist.local)
     torch.cuda.set_device(dev)
-    w0 = W.WORKLOADS[args.config]
+    w0 = W.WORKLOADS[config]
     w, host, d = make_inputs(w0, dev, dist.rank)
     step = TreeVerifyStep.for_workload(w, dev)
     stream = torch.cuda.Stream(device=dev)
@@ -409,13 +418,14 @@ def run_ours(args, dist):
                 for j, c in enumerate(calls)}
     err_word = int(step.err[0].item())
 
-    # ---- e2e: host buffers through the Python API ----
-    e2e = run_e2e(args, step, host, d, dev, stream, plen0)
-
-    # ---- cost-aware adaptive budget (tsd_tree_build_adaptive) ----
-    adaptive = run_adaptive(args, w, step, d, dev, stream)
-    # ---- the same verify through a shuffled page pool ----
-    paged = run_paged(args, w, step, d, dev, stream, plen0)
+    e2e = adaptive = paged = None
+    if not lite:
+        # ---- e2e: host buffers through the Python API ----
+        e2e = run_e2e(args, step, host, d, dev, stream, plen0)
+        # ---- cost-aware adaptive budget (tsd_tree_build_adaptive) ----
+        adaptive = run_adaptive(args, w, step, d, dev, stream)
+        # ---- the same verify through a shuffled page pool ----
+        paged = run_paged(args, w, step, d, dev, stream, plen0)
 
     nodes = w.B * w.D
     value = nodes * dist.world / (ms / 1e3)
@@ -426,7 +436,7 @@ def run_ours(args, dist):
     # latent heads: the verify call is a dense contraction (about 2200 flop per
     # byte of KV), so its roofline is the tensor pipe
     tensor_bound = w.v_aliases_k and dominant == "verify"
-    traffic = load_traffic().get(f"{args.config}:{dominant}")
+    traffic = load_traffic().get(f"{config}:{dominant}")
     traffic_val = None
     if traffic and traffic.get("digest") == source_digest(CALL_SOURCES[dominant]):
         traffic_val = traffic.get("bytes_per_launch")
@@ -454,6 +464,7 @@ def run_ours(args, dist):
                      "algorithmic_bytes_per_launch": algo[dominant], "traffic": traffic_val},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
+        "launches_per_step": launches_per_step,
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 4),
         "device_err_word": err_word,
@@ -471,6 +482,11 @@ def run_ours(args, dist):
                             if tkind == "measured" else "fallback 1.9 PF/s",
                             "algorithmic_flops_per_launch": fl, "traffic": traffic_val,
                             "algorithmic_bytes_per_launch": algo["verify"]}
+    if lite:
+        for key in ("e2e", "adaptive", "paged", "gpu_launches", "wall_s_timed_region"):
+            line.pop(key, None)
+    del step, d
+    torch.cuda.empty_cache()
     return line, w, host
 
 
@@ -748,6 +764,15 @@ def main():
                 print(json.dumps(line), flush=True)
             return
         line, w, host = run_ours(args, dist)
+        also = [c for c in args.also.split(",") if c and c != args.config]
+        if also:
+            line["also"] = {}
+            for c in also:
+                sub, _, _ = run_ours(args, dist, config=c, lite=True)
+                line["also"][c] = {k: sub[k] for k in (
+                    "value", "unit", "ms_per_step", "config", "step_latency_us", "per_call_us",
+                    "attn_kv_gbs", "attn_kv_frac_of_hbm", "roofline", "clocks",
+                    "device_err_word", "launches_per_step")}
         if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, host, args.cpu_seconds)
         elif dist.rank == 0:

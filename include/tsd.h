@@ -77,6 +77,7 @@ typedef enum {
 #define TSD_DEV_ERR_BAD_TREE 0x02000000 /* parent/row out of range, walk deeper than S */
 #define TSD_DEV_ERR_TIMEOUT  0x03000000 /* a bounded wait inside a kernel gave up */
 #define TSD_DEV_ERR_BAD_PAGE 0x04000000 /* page table entry outside the page pool */
+#define TSD_DEV_ERR_BAD_PROBS 0x05000000 /* a draft probability above 1 or NaN */
 #define TSD_DEV_ERR_MASK     0x7f000000
 
 /* Element types of attention operands. */
@@ -95,8 +96,12 @@ int tsd_version(void);
  * Per-position top-k then greedy best-first tree ("Cost-Aware Diffusion Draft
  * Trees", Method 2; V4 review, toy steps 1-2).
  *
- * probs     [B][S][V] fp32: the draft's per-position marginal distributions
- *           (non-negative, no NaN; -0.0 counts as +0.0).
+ * probs     [B][S][V] fp32: the draft's per-position marginal distributions,
+ *           values in [0, 1] (-0.0 counts as +0.0).  The best-first order
+ *           relies on a child's score never exceeding its parent's, i.e. on
+ *           p <= 1: a row holding a value above 1 or a NaN sets
+ *           TSD_DEV_ERR_BAD_PROBS | b in err (the first error wins), and that
+ *           request's tree is then unspecified (it is still a valid tree).
  * root_tok  [B] int32: the root (anchor) token of each request.
  * Outputs, all [B][1+D]:
  *   token   int32  row's token (row 0 = root_tok)
@@ -338,9 +343,12 @@ tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, int V,
  * whose tsd_accept_walk_workspace_size(B, D, V) exceeds 1 MiB returns
  * TSD_ERR_UNSUPPORTED.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress), so make that first call before any stream
- * capture.  Calls that overlap on the GPU (on different streams) share the
- * array and race.  Nothing in the array needs to start at zero.  The call
- * allocates and frees nothing.
+ * capture.  The address is kept per device and looked up again when the
+ * device's current context changes (a cudaDeviceReset gives the device a new
+ * context and the array a new address): the first call after such a reset
+ * must also come before any capture.  Calls that overlap on the GPU (on
+ * different streams) share the array and race.  Nothing in the array needs
+ * to start at zero.  The call allocates and frees nothing.
  * -------------------------------------------------------------------------- */
 tsd_status tsd_accept_walk_static(const float* logits, int B, int D, int S, int V,
                                   const int32_t* token, const int32_t* parent,

@@ -714,17 +714,46 @@ def test_cost_model_calibrated_on_this_gpu():
 
 # ------------------------------------------------ one graph per round --
 
-@pytest.mark.parametrize("adaptive", [False, True])
-def test_captured_round_matches_eager_calls(adaptive):
-    """The whole round recorded as one CUDA graph gives bit-identical trees,
-    attention, walk and committed cache to the eager calls, replay after
-    replay (inputs refilled in place between replays)."""
-    d = inputs("batched", B=4, P=600, P_min=200, V=4000)
-    w, tree = d["w"], d["tree"]
+def _oracle_round(w, d, tree, q, kc, vc, plen, kt, vt, tl, sel):
+    """The oracle's view of one whole round on these inputs: sampled attention
+    rows, argmax, walk, and the cache and prefix lengths after the commit."""
+    ref_out, _ = oracle.verify_attn(W.bits(q), W.bits(kc), None if vc is None else W.bits(vc),
+                                    plen.numpy(), W.bits(kt), None if vt is None else W.bits(vt),
+                                    tree["mask"], w.scale, v_aliases_k=w.v_aliases_k, dv=w.dv,
+                                    sel=sel)
+    tgt = oracle.argmax(tl.numpy())
+    walk = oracle.accept_walk(tgt, tree, w.S)
+    kc_ref = W.bits(kc).copy()
+    vc_ref = None if vc is None else W.bits(vc).copy()
+    pl_ref = plen.numpy().copy()
+    oracle.commit(W.bits(kt), None if vt is None else W.bits(vt), walk["accept_rows"],
+                  walk["accept_len"], kc_ref, vc_ref, pl_ref, w.S, v_aliases_k=w.v_aliases_k)
+    return ref_out, tgt, walk, kc_ref, vc_ref, pl_ref
+
+
+@pytest.mark.parametrize("case", ["batched", "batched_adaptive", "qwen"])
+def test_captured_round_matches_oracle(case):
+    """The whole round recorded as one CUDA graph (TreeVerifyStep.capture, the
+    flow the benchmark times) matches the oracle replay after replay -- tree,
+    sampled attention rows, argmax, walk, committed cache and prefix lengths
+    -- and is bit-identical to the eager calls.  "qwen" is the benchmark's own
+    graph: the full qwen workload."""
+    adaptive = case.endswith("adaptive")
+    d = inputs("qwen") if case == "qwen" else inputs("batched", B=4, P=600, P_min=200, V=4000)
+    w = d["w"]
     q, kc, vc, plen, kt, vt = attn_inputs(w)
+    if adaptive:
+        cd, cv = _cost_tables(w, "mid", seed=2)
+        tree = oracle.tree_adaptive(d["tp"], d["ti"], w.D, d["root"].numpy(), cd, cv,
+                                    method="beam")
+        extra = (torch.from_numpy(cd).to(DEV), torch.from_numpy(cv).to(DEV))
+    else:
+        tree = d["tree"]
+        extra = (None, None)
     tl = W.target_logits(w, torch.from_numpy(tree["depth"]), d["logits"])
-    cd, cv = _cost_tables(w, "mid", seed=2) if adaptive else (None, None)
-    extra = (torch.from_numpy(cd).to(DEV), torch.from_numpy(cv).to(DEV)) if adaptive else (None, None)
+    sel = sample_rows(w, 24, seed=3)
+    ref_out, tgt, walk, kc_ref, vc_ref, pl_ref = _oracle_round(w, d, tree, q, kc, vc, plen, kt,
+                                                               vt, tl, sel)
 
     def fresh():
         return gpu(d["probs"], d["root"], q, kc.clone(), None if vc is None else vc.clone(),
@@ -739,24 +768,64 @@ def test_captured_round_matches_eager_calls(adaptive):
     gg = fresh()
     g = graphed.capture(*gg, *extra)
     for _ in range(2):
-        # restore the state the eager round started from, then replay
+        # restore the state the round started from, then replay
         gg[3].copy_(kc.to(DEV))
         if vc is not None:
             gg[4].copy_(vc.to(DEV))
         gg[5].copy_(plen.to(DEV))
         g.replay()
         torch.cuda.synchronize()
+        t = graphed.tree
+        got = dict(token=t.token.cpu().numpy(), parent=t.parent.cpu().numpy(),
+                   depth=t.depth.cpu().numpy(), score=t.score.cpu().numpy(),
+                   mask=t.mask.cpu().numpy().view(np.uint64), is_leaf=t.is_leaf.cpu().numpy())
+        assert_tree_equal(got, tree)
+        if adaptive:
+            np.testing.assert_array_equal(graphed.n_nodes.cpu().numpy(), tree["n_nodes"])
+        out = graphed.out.float().cpu().numpy()
+        err = np.abs(np.stack([out[b, r, h] for b, r, h in sel]) - ref_out).max()
+        assert err <= _tol(w), f"attention max abs err {err}"
+        wk = graphed.walk
+        np.testing.assert_array_equal(wk.tgt.cpu().numpy(), tgt)
+        for key in ("accept_len", "accept_rows", "bonus", "chain_id"):
+            np.testing.assert_array_equal(getattr(wk, key).cpu().numpy(), walk[key])
+        np.testing.assert_array_equal(W.bits(gg[3].cpu()), kc_ref)
+        if vc is not None:
+            np.testing.assert_array_equal(W.bits(gg[4].cpu()), vc_ref)
+        np.testing.assert_array_equal(gg[5].cpu().numpy(), pl_ref)
+        # and the same bytes as the eager calls
         for f in ("token", "parent", "depth", "score", "mask", "is_leaf"):
             assert torch.equal(getattr(eager.tree, f), getattr(graphed.tree, f)), f
         assert torch.equal(eager.out, graphed.out) and torch.equal(eager.lse, graphed.lse)
         for f in ("tgt", "accept_len", "accept_rows", "bonus", "chain_id"):
             assert torch.equal(getattr(eager.walk, f), getattr(graphed.walk, f)), f
         assert torch.equal(ge[3], gg[3]) and torch.equal(ge[5], gg[5])
-        if vc is not None:
-            assert torch.equal(ge[4], gg[4])
-        if adaptive:
-            assert torch.equal(eager.n_nodes, graphed.n_nodes)
     assert int(graphed.err[0]) == 0
+
+
+def test_tree_build_reports_probabilities_above_one_or_nan():
+    """A draft row with a value above 1 or a NaN breaks the score order the
+    best-first rule needs: the build reports it in the error word (the first
+    error wins) and builds the other requests' trees exactly."""
+    d = inputs("qwen", B=3, V=3000)
+    w = d["w"]
+    for bad_b, val in [(1, 1.5), (2, float("nan")), (0, float("inf"))]:
+        probs = d["probs"].clone()
+        probs[bad_b, 3, 1234] = val
+        step = TreeVerifyStep.for_workload(w, DEV)
+        got = run_tree(step, probs, d["root"])
+        assert int(step.err[0]) == (T.TSD_DEV_ERR_BAD_PROBS | bad_b), val
+        for b in range(w.B):
+            if b == bad_b:
+                continue
+            for key in ("token", "parent", "depth", "is_leaf", "mask"):
+                np.testing.assert_array_equal(got[key][b], d["tree"][key][b], err_msg=key)
+    step = TreeVerifyStep.for_workload(w, DEV)
+    probs = d["probs"].clone()
+    probs[0, 0, 7] = 1.0          # exactly 1 is allowed
+    probs[1, 2, 9] = -0.0
+    run_tree(step, probs, d["root"])
+    assert int(step.err[0]) == 0
 
 
 # ------------------------------------------- parent-conditioned proposals --

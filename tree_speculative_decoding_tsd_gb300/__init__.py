@@ -38,6 +38,7 @@ TSD_ERR_DEVICE_TIMEOUT = 5
 TSD_DEV_ERR_CAPACITY = 0x01000000
 TSD_DEV_ERR_BAD_TREE = 0x02000000
 TSD_DEV_ERR_BAD_PAGE = 0x04000000
+TSD_DEV_ERR_BAD_PROBS = 0x05000000
 TSD_DEV_ERR_TIMEOUT = 0x03000000
 TSD_DEV_ERR_MASK = 0x7F000000
 TSD_F32 = 0

@@ -19,6 +19,8 @@
 #include "tsd_host.h"
 #include "tsd_scan.cuh"
 
+#include <cuda.h>
+
 #include <mutex>
 
 namespace tsd {
@@ -159,7 +161,7 @@ extern "C" tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, 
   const ScanGeom g = scan_geometry(rows, V, 1, true);
   uint64_t* part = (uint64_t*)ws;
   launch(vocab_scan_kernel<true>, dim3((unsigned)(rows * g.nchunk)), dim3(kScanThreads), 0, st,
-      logits, V, 1, g.nchunk, g.chunk_len, part, g.one_wave);
+      logits, V, 1, g.nchunk, g.chunk_len, part, g.one_wave, nullptr, 1);
   launch(accept_walk_kernel, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk, token,
       parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err);
   return cuda_status();
@@ -182,20 +184,46 @@ namespace {
 constexpr size_t kWalkStaticScratchBytes = size_t(1) << 20;  // 1 MiB
 static __device__ __align__(256) uint64_t g_walk_static_scratch[kWalkStaticScratchBytes / 8];
 
-// Device address of the array on the current device.  In host code the
+// Device address of the array in the current context.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up with
-// cudaGetSymbolAddress once per device (the first call on a device does it).
+// cudaGetSymbolAddress; the first call on a device does it, and it is looked
+// up again whenever the device's current context is a different one (after a
+// cudaDeviceReset the array lives in the new context).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (CtxGetCurrentFn)p;
+  });
+  return fn;
+}
+
 uint64_t* walk_static_scratch() {
   constexpr int kMaxDevices = 64;
   static uint64_t* addr[kMaxDevices] = {};
+  static CUcontext owner[kMaxDevices] = {};
   static std::mutex mu;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  CUcontext ctx = nullptr;
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (get != nullptr && get(&ctx) != CUDA_SUCCESS) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || ctx == nullptr || owner[dev] != ctx) {
+    // (the lookup makes the device's primary context current if none is)
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_walk_static_scratch) != cudaSuccess) return nullptr;
     addr[dev] = (uint64_t*)p;
+    ctx = nullptr;
+    if (get != nullptr) get(&ctx);
+    owner[dev] = ctx;
   }
   return addr[dev];
 }
@@ -229,7 +257,7 @@ extern "C" tsd_status tsd_accept_walk_static(const float* logits, int B, int D, 
   const long rows = (long)B * R;
   const ScanGeom g = scan_geometry(rows, V, 1, true);
   launch(vocab_scan_kernel<true>, dim3((unsigned)(rows * g.nchunk)), dim3(kScanThreads), 0, st,
-      logits, V, 1, g.nchunk, g.chunk_len, part, g.one_wave);
+      logits, V, 1, g.nchunk, g.chunk_len, part, g.one_wave, nullptr, 1);
   launch(accept_walk_kernel, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk, token,
       parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err);
   return cuda_status();

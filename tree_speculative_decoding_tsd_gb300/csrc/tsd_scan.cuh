@@ -15,6 +15,9 @@
 // L2, where the first pass left them) and offers the ones >= T to a sorted
 // warp list; the CTA then merges its eight warp lists.  NaN entries are never
 // selected.
+// Top-k mode also checks that the row is a probability vector as the tree
+// rule needs it (no value above 1, no NaN) and reports a violation in the
+// caller's error word.
 // Argmax mode (k = 1) keeps one running maximum per thread.
 #pragma once
 
@@ -68,10 +71,18 @@ inline ScanGeom scan_geometry(long rows, int V, int k, bool argmax) {
 
 __device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
 
+// max(a, b, c) that returns NaN if any operand is NaN (three-operand
+// max.NaN.f32, sm_100 and later)
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <bool kArgmax>
 __global__ void __launch_bounds__(kScanThreads, kArgmax ? kScanArgmaxPerSm : kScanTopkPerSm)
 vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chunk_len,
-                  uint64_t* __restrict__ out, int prefetch) {
+                  uint64_t* __restrict__ out, int prefetch, int32_t* err, int rows_per_req) {
   __shared__ uint64_t s_list[kScanWarps][32];
   __shared__ float s_max[kScanThreads];
   __shared__ float s_cut;
@@ -147,7 +158,8 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
 
   // ---- top-k mode -------------------------------------------------------
   // pass 1: stream the vector part once, one running maximum per thread
-  float m = -INFINITY;
+  // (NaN ignored), and one that keeps NaN (for the range check)
+  float m = -INFINITY, mn = -INFINITY;
   {
     int v = tid;
     for (; v + 3 * kScanThreads < nvec; v += 4 * kScanThreads) {
@@ -155,18 +167,26 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
 #pragma unroll
       for (int u = 0; u < 4; ++u) f[u] = __ldg(xv + v + u * kScanThreads);
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 4; ++u) {
         m = fmaxf(m, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
+        mn = max3_nan(mn, max3_nan(f[u].x, f[u].y, f[u].z), f[u].w);
+      }
     }
 #pragma unroll
     for (int u = 0; u < 3; ++u) {
       if (v + u * kScanThreads < nvec) {
         const float4 f = __ldg(xv + v + u * kScanThreads);
         m = fmaxf(m, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+        mn = max3_nan(mn, max3_nan(f.x, f.y, f.z), f.w);
       }
     }
   }
   s_max[tid] = m;
+  for (int i = c0 + tid; i < a0; i += kScanThreads) mn = max3_nan(mn, xr[i], -INFINITY);
+  for (int i = a1 + tid; i < c1; i += kScanThreads) mn = max3_nan(mn, xr[i], -INFINITY);
+  // a value above 1 (or NaN) breaks the score order the tree build relies on
+  if (err != nullptr && __any_sync(kFull, !(mn <= 1.0f)) && lane == 0)
+    report_error(err, TSD_DEV_ERR_BAD_PROBS, (int)(row / rows_per_req));
 
   // the (at most 3 + 3) scalar edge elements are offered to the warp list directly
   const unsigned kmask = (k >= 32) ? kFull : ((1u << k) - 1u);

@@ -309,13 +309,14 @@ tsd_status tree_build_impl(const float* probs, int B, int S, int V, int k, int D
                            const int32_t* root_tok, const float* cost_d, const float* cost_v,
                            int32_t* token, int32_t* parent, int32_t* depth, float* score,
                            uint64_t* mask, uint8_t* is_leaf, int32_t* n_nodes, void* ws,
-                           size_t ws_bytes, tsd_stream_t stream) {
+                           size_t ws_bytes, int32_t* err, tsd_stream_t stream) {
   if (B < 1 || S < 1 || S > kMaxS || k < 1 || k > kMaxK || V < k || D < 1 || D > kMaxD)
     return TSD_ERR_INVALID_ARG;
   if (tree_node_count(S, k) < D) return TSD_ERR_INVALID_ARG;
   if ((long)B * S > (1l << 24) || (long)V > (1l << 30)) return TSD_ERR_INVALID_ARG;
   if (!ok_ptr(probs) || !ok_ptr(root_tok) || !ok_ptr(token) || !ok_ptr(parent) ||
-      !ok_ptr(depth) || !ok_ptr(score) || !ok_ptr(mask) || !ok_ptr(is_leaf))
+      !ok_ptr(depth) || !ok_ptr(score) || !ok_ptr(mask) || !ok_ptr(is_leaf) ||
+      (((uintptr_t)err) & 3u) != 0)
     return TSD_ERR_INVALID_ARG;
   const size_t need = tsd_tree_build_workspace_size(B, S, V, k);
   if (ws_bytes < need || !ok_ptr(ws)) return TSD_ERR_INVALID_ARG;
@@ -325,7 +326,7 @@ tsd_status tree_build_impl(const float* probs, int B, int S, int V, int k, int D
   const long ctas = (long)B * S * g.nchunk;
   uint64_t* part = (uint64_t*)ws;
   launch(vocab_scan_kernel<false>, dim3((unsigned)ctas), dim3(kScanThreads), 0, st, probs, V, k,
-      g.nchunk, g.chunk_len, part, g.one_wave);
+      g.nchunk, g.chunk_len, part, g.one_wave, err, S);
   const auto tree_kernel = D + 2 <= 32   ? best_first_tree_kernel<1>
                            : D + 2 <= 64 ? best_first_tree_kernel<2>
                                          : best_first_tree_kernel<3>;
@@ -341,9 +342,8 @@ extern "C" tsd_status tsd_tree_build(const float* probs, int B, int S, int V, in
                                      int32_t* depth, float* score, uint64_t* mask,
                                      uint8_t* is_leaf, void* ws, size_t ws_bytes, int32_t* err,
                                      tsd_stream_t stream) {
-  (void)err;
   return tree_build_impl(probs, B, S, V, k, D, root_tok, nullptr, nullptr, token, parent, depth,
-                         score, mask, is_leaf, nullptr, ws, ws_bytes, stream);
+                         score, mask, is_leaf, nullptr, ws, ws_bytes, err, stream);
 }
 
 extern "C" tsd_status tsd_tree_build_adaptive(const float* probs, int B, int S, int V, int k,
@@ -353,8 +353,7 @@ extern "C" tsd_status tsd_tree_build_adaptive(const float* probs, int B, int S, 
                                               float* score, uint64_t* mask, uint8_t* is_leaf,
                                               int32_t* n_nodes, void* ws, size_t ws_bytes,
                                               int32_t* err, tsd_stream_t stream) {
-  (void)err;
   if (!ok_ptr(cost_d) || !ok_ptr(cost_v) || !ok_ptr(n_nodes)) return TSD_ERR_INVALID_ARG;
   return tree_build_impl(probs, B, S, V, k, D_max, root_tok, cost_d, cost_v, token, parent, depth,
-                         score, mask, is_leaf, n_nodes, ws, ws_bytes, stream);
+                         score, mask, is_leaf, n_nodes, ws, ws_bytes, err, stream);
 }
