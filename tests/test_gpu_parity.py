@@ -145,6 +145,7 @@ def check_attention(w, q, kc, vc, plen, kt, vt, mask, sel=None):
     step.tree.mask.copy_(torch.from_numpy(np.ascontiguousarray(mask).view(np.int64)))
     step.verify(*gpu(q, kc, vc, plen, kt, vt))
     torch.cuda.synchronize()
+    assert int(step.err[0]) == 0, hex(int(step.err[0]))   # no bounded wait gave up
     out = step.out.float().cpu().numpy().astype(np.float64)
     lse = step.lse.cpu().numpy().astype(np.float64)
     ref_out, ref_lse = oracle.verify_attn(W.bits(q), W.bits(kc), None if vc is None else W.bits(vc),

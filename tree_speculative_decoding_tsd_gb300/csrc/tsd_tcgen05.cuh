@@ -76,6 +76,14 @@ __device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* map, int
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_5d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                       int w, int v, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(map),
                "r"(x), "r"(y), "r"(z)

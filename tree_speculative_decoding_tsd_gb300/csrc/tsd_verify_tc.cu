@@ -98,7 +98,7 @@ struct TcLayout {
   static constexpr uint32_t off_rmask = (off_shift + 4 * N + 7) / 8 * 8;  // u64[N] tree masks
   static constexpr uint32_t off_ooff = off_rmask + 8 * N;           // i64[N] output offsets
   static constexpr uint32_t off_bar = off_ooff + 8 * N;             // mbarriers
-  static constexpr int nbar = 16;
+  static constexpr int nbar = 17;
   static constexpr uint32_t off_flags = off_bar + 8 * nbar;          // tmem addr, abort flag
   static constexpr uint32_t off_tiles = off_flags + 16;  // int[kPagedTiles] tile rows (paged)
   static constexpr uint32_t total = off_tiles + 4 * kPagedTiles;
@@ -109,13 +109,17 @@ struct TcLayout {
   }
 };
 
-// barrier indices
-// (BAR_PV_DONE completes once per O^T product; a softmax warp waits on it only
+// Barrier indices.  K_FULL/K_EMPTY per K stage, V_FULL/V_EMPTY per V stage,
+// S_FULL per S^T buffer, P_FULL per tile parity, PV_DONE per O^T product,
+// O_DONE once after the last O^T product.
+// A warpgroup may run one tile ahead of another (S^T_(t+1) is issued before
+// O^T_t), never two (S^T_(t+2) waits for P_FULL_t): the 16 softmax warps'
+// arrivals for tile t go to the P_FULL barrier of t's parity, so an early
+// arrival for t+1 never counts toward t.  A softmax warp waits on PV_DONE only
 // from tile t, when products 0..t-2 are known complete, so its parity is
-// unambiguous.  The epilogue waits on BAR_O_DONE, committed once after the
-// last product.)
+// unambiguous; the epilogue waits on O_DONE.
 enum { BAR_K_FULL = 0, BAR_K_EMPTY = 3, BAR_V_FULL = 6, BAR_V_EMPTY = 8, BAR_S_FULL = 10,
-       BAR_P_FULL = 12, BAR_PV_DONE = 13, BAR_FINAL = 14, BAR_O_DONE = 15 };
+       BAR_P_FULL = 12, BAR_PV_DONE = 14, BAR_FINAL = 15, BAR_O_DONE = 16 };
 
 struct TcMaps {
   CUtensorMap k, v, kt, vt;
@@ -236,6 +240,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       mbar_init(bar(BAR_S_FULL + s2), 1);
     }
     mbar_init(bar(BAR_P_FULL), kSoftWarps);
+    mbar_init(bar(BAR_P_FULL + 1), kSoftWarps);
     mbar_init(bar(BAR_PV_DONE), 1);
     mbar_init(bar(BAR_FINAL), 1);
     mbar_init(bar(BAR_O_DONE), 1);
@@ -363,7 +368,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       bool ok = issue_qk(0);
       for (int t = 0; ok && t < ntiles; ++t) {
         if (t + 1 < ntiles && !issue_qk(t + 1)) { ok = false; break; }
-        if (!mbar_wait(bar(BAR_P_FULL), t & 1) || flags[1]) { ok = false; break; }
+        if (!mbar_wait(bar(BAR_P_FULL + (t & 1)), (t >> 1) & 1) || flags[1]) { ok = false; break; }
         if (!mbar_wait(bar(BAR_V_FULL + (t & 1)), (t >> 1) & 1)) { ok = false; break; }
         fence_after();
         const int stg = t % kKStages;
@@ -601,7 +606,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_P_FULL));
+      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + (t & 1)));
     }
 
     // ---------------------------------------------------------- epilogue
