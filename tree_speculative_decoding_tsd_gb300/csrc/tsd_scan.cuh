@@ -159,26 +159,31 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
   // ---- top-k mode -------------------------------------------------------
   // pass 1: stream the vector part once, one running maximum per thread
   // (NaN ignored), and one that keeps NaN (for the range check)
+  // (eight 16-byte loads in flight per thread: with about three CTAs per SM
+  // that is what keeps enough bytes in flight to stream at HBM speed)
   float m = -INFINITY, mn = -INFINITY;
   {
+    constexpr int U = 8;
     int v = tid;
-    for (; v + 3 * kScanThreads < nvec; v += 4 * kScanThreads) {
-      float4 f[4];
+    for (; v + (U - 1) * kScanThreads < nvec; v += U * kScanThreads) {
+      float4 f[U];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) f[u] = __ldg(xv + v + u * kScanThreads);
+      for (int u = 0; u < U; ++u) f[u] = __ldg(xv + v + u * kScanThreads);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < U; ++u) {
         m = fmaxf(m, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
         mn = max3_nan(mn, max3_nan(f[u].x, f[u].y, f[u].z), f[u].w);
       }
     }
+    float4 f[U - 1];
 #pragma unroll
-    for (int u = 0; u < 3; ++u) {
-      if (v + u * kScanThreads < nvec) {
-        const float4 f = __ldg(xv + v + u * kScanThreads);
-        m = fmaxf(m, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
-        mn = max3_nan(mn, max3_nan(f.x, f.y, f.z), f.w);
-      }
+    for (int u = 0; u < U - 1; ++u)
+      f[u] = v + u * kScanThreads < nvec ? __ldg(xv + v + u * kScanThreads)
+                                         : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll
+    for (int u = 0; u < U - 1; ++u) {
+      m = fmaxf(m, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
+      mn = max3_nan(mn, max3_nan(f[u].x, f[u].y, f[u].z), f[u].w);
     }
   }
   s_max[tid] = m;

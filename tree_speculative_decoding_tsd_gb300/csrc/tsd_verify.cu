@@ -159,7 +159,7 @@ verify_generic_kernel(const __grid_constant__ VerifyArgs a) {
     const int p = rg * RB + i;
     const int r = p / a.g, h = hk * a.g + p % a.g;
     const long orow = ((long)b * a.R + r) * a.Hq + h;
-    if (a.nsplit == 1) {
+    if (nsb == 1) {
       ((T*)a.out)[orow * DV + c] = cvt_out<T>(res);
       if (c == 0) a.lse[orow] = lse2 * 0.69314718055994531f;
     } else {

@@ -161,7 +161,9 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, int b, int r, 
   if (lane == 0) a.lse[row] = tot * 0.69314718055994531f;
 }
 
-// Split merge: one warp per output row ((b*R + r)*Hq + h), spread over the
+// Split merge: one warp per output row ((b*R + r)*Hq + h) of a request whose
+// prefix spans several splits (a request held by one split is written
+// directly by the attention kernel), spread over the
 // whole GPU (merging in the last CTA of each request and head instead left
 // one CTA with a serial tail of dependent loads: 10% slower attention on every
 // workload).  It is launched with ordinary stream serialisation: launched
@@ -179,6 +181,7 @@ verify_combine_kernel(const __grid_constant__ VerifyArgs a) {
   const int h = (int)(row % a.Hq);
   const int P = min(max(a.plen[b], 0), a.cap);
   const int nsb = P > 0 ? (P + a.split_len - 1) / a.split_len : 1;
+  if (nsb == 1) return;   // a request held by one split wrote its output directly
   merge_splits<T, DV>(a, b, r, h, nsb, lane);
 }
 

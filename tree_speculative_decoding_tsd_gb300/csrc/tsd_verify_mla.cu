@@ -573,7 +573,7 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, const __grid_constant__ 
           const int p = row_base + col;
           const int tr = p / a.g, qh = hk * a.g + p % a.g;
           const float lse2 = m_run[col] + log2f(ls);
-          if (a.nsplit == 1) {
+          if (nsb == 1) {
             const long orow = ((long)b * a.R + tr) * a.Hq + qh;
             ooff[col] = orow * kDV;
             a.lse[orow] = lse2 * 0.69314718055994531f;
@@ -598,7 +598,7 @@ verify_mla_kernel(const __grid_constant__ MlaMaps maps, const __grid_constant__ 
             const int col = c0 + 4 * j + i;
             if (col >= rows_here) break;
             const float res = v[i] * alpha[col];
-            if (a.nsplit == 1) ((__nv_bfloat16*)a.out)[ooff[col] + d] = __float2bfloat16_rn(res);
+            if (nsb == 1) ((__nv_bfloat16*)a.out)[ooff[col] + d] = __float2bfloat16_rn(res);
             else a.ws_o[ooff[col] + d] = res;
           }
         }

@@ -267,7 +267,7 @@ verify_mma_kernel(const __grid_constant__ VerifyArgs a, int rows_per_cta) {
     const int tr = i == 0 ? tr0 : tr1, qh = i == 0 ? qh0 : qh1;
     const float inv = 1.f / lrow[i];
     const float lse2 = mrow[i] + log2f(lrow[i]);
-    if (a.nsplit == 1) {
+    if (nsb == 1) {
       const long orow = ((long)b * a.R + tr) * a.Hq + qh;
       uint32_t* dst = (uint32_t*)((__nv_bfloat16*)a.out + orow * DK);
 #pragma unroll
