@@ -258,6 +258,18 @@ tsd_status tsd_tree_verify_attn(const tsd_attn_desc* desc, const void* q,
  * the previous setting, or -1 (and changes nothing) for an unknown path. */
 int tsd_set_verify_path(int path);
 
+/* Diagnostic: the budget, in SM clock cycles, of the pipeline waits inside
+ * the tcgen05 attention kernel of bf16 heads for the verify calls that follow
+ * (the waits on its copy, product and softmax stages; the final waits that
+ * let copies and products in flight land before the kernel exits keep the
+ * default of about one second).  0 restores the default; a positive budget
+ * below it makes those waits poll without sleeping and give up once it is
+ * spent, after which the kernel writes no output for the CTA's rows and sets
+ * TSD_DEV_ERR_TIMEOUT | b in err -- the path a stalled copy or product takes,
+ * made reachable without a fault.  No counterpart on the pages.  Process-wide,
+ * like tsd_set_verify_path.  Returns the previous setting (0 = default). */
+long long tsd_set_wait_budget(long long cycles);
+
 /* --------------------------------------------------------------------------
  * Paged KV cache: tsd_tree_verify_attn_paged, tsd_commit_path_paged
  *

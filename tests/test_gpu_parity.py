@@ -514,6 +514,39 @@ def test_verify_each_path_reduced(force_path, key):
     check_attention(w, *attn_inputs(w), d["tree"]["mask"])
 
 
+def test_verify_bounded_wait_gives_up_then_next_call_is_exact():
+    """A pipeline-wait budget of a few clock cycles makes the tcgen05 kernel's
+    first wait on a product give up (the waits poll instead of sleeping):
+    each CTA skips its output and exits once its copies and products in flight
+    have landed and its TMEM is released, and the first one records
+    TSD_DEV_ERR_TIMEOUT | b.  With the default budget restored, the next call
+    on the same buffers is within tolerance of the oracle, and the one after
+    that on a fresh step too."""
+    d = inputs("qwen", **REDUCED["qwen"])
+    w = d["w"]
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    step = TreeVerifyStep.for_workload(w, DEV)
+    step.tree.mask.copy_(torch.from_numpy(np.ascontiguousarray(d["tree"]["mask"]).view(np.int64)))
+    args = gpu(q, kc, vc, plen, kt, vt)
+    with T.verify_path("tc"):
+        with T.wait_budget(16):
+            step.verify(*args)
+            torch.cuda.synchronize()
+        e = int(step.err[0])
+        assert e & T.TSD_DEV_ERR_MASK == T.TSD_DEV_ERR_TIMEOUT, hex(e)
+        assert 0 <= (e & 0xFFFFFF) < w.B
+        assert T.tsd_set_wait_budget(0) == 0           # the context manager restored it
+        step.err.zero_()
+        step.verify(*args)
+        torch.cuda.synchronize()
+        assert int(step.err[0]) == 0
+        ref_out, _ = oracle.verify_attn(W.bits(q), W.bits(kc), W.bits(vc), plen.numpy(), W.bits(kt),
+                                        W.bits(vt), d["tree"]["mask"], w.scale)
+        err = np.abs(step.out.float().cpu().numpy().astype(np.float64) - ref_out).max()
+        assert err <= _tol(w), f"max abs err {err}"
+        check_attention(w, q, kc, vc, plen, kt, vt, d["tree"]["mask"])
+
+
 @pytest.mark.parametrize("force_path", ["tc"], indirect=True)
 @pytest.mark.parametrize("D", [3, 5, 7, 11])
 def test_verify_tcgen05_small_trees(force_path, D):

@@ -51,7 +51,7 @@ EXPORTED = ("tsd_status_string", "tsd_version", "tsd_tree_build_workspace_size",
             "tsd_verify_workspace_size",
             "tsd_tree_verify_attn", "tsd_tree_verify_attn_paged", "tsd_commit_path_paged",
             "tsd_accept_walk_workspace_size", "tsd_accept_walk", "tsd_accept_walk_static",
-            "tsd_commit_path", "tsd_set_verify_path")
+            "tsd_commit_path", "tsd_set_verify_path", "tsd_set_wait_budget")
 
 
 class TsdError(RuntimeError):
@@ -105,6 +105,8 @@ def _load():
     lib.tsd_commit_path_paged.restype = I
     lib.tsd_set_verify_path.argtypes = [I]
     lib.tsd_set_verify_path.restype = I
+    lib.tsd_set_wait_budget.argtypes = [ctypes.c_longlong]
+    lib.tsd_set_wait_budget.restype = ctypes.c_longlong
     return lib
 
 
@@ -147,6 +149,30 @@ class verify_path:
 
     def __exit__(self, *exc):
         tsd_set_verify_path(self.prev)
+        return False
+
+
+def tsd_set_wait_budget(cycles: int) -> int:
+    """Budget (SM clock cycles) of the tcgen05 verify kernel's pipeline waits
+    for the calls that follow; 0 restores the default.  Returns the previous
+    setting."""
+    if int(cycles) < 0:
+        raise ValueError("wait budget must be >= 0")
+    return int(_L().tsd_set_wait_budget(int(cycles)))
+
+
+class wait_budget:
+    """Context manager: the verify calls inside use the given wait budget."""
+
+    def __init__(self, cycles):
+        self.cycles = cycles
+
+    def __enter__(self):
+        self.prev = tsd_set_wait_budget(self.cycles)
+        return self
+
+    def __exit__(self, *exc):
+        tsd_set_wait_budget(self.prev)
         return False
 
 

@@ -10,6 +10,11 @@ namespace tsd {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// Default budget of every bounded device wait (an mbarrier or a flag), in SM
+// clock cycles: about one second at 2 GHz.  A wait that runs out records
+// TSD_DEV_ERR_TIMEOUT and its kernel returns instead of hanging.
+constexpr long long kWaitCycles = 2000000000ll;
+
 // Order-preserving map of an fp32 value to uint32 (larger float -> larger
 // key).  -0.0 is folded onto +0.0 so that the two compare equal, as they do
 // for float comparison.

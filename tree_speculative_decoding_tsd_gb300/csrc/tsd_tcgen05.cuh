@@ -15,7 +15,6 @@
 
 namespace tsd {
 
-constexpr long long kWaitCycles = 2000000000ll;  // bounded waits: ~1 s at 2 GHz
 
 namespace {
 
@@ -31,12 +30,33 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-// Bounded wait for the phase with the given parity; false on timeout.  Each
-// try_wait carries a suspend-time hint (in ns), so a waiting warp sleeps until
-// the phase completes instead of spinning on issue slots that the warps
-// sharing its scheduler need; the hint is far below the overall budget.
+// Bounded wait for the phase with the given parity; false once `budget`
+// clock cycles have passed.  Each try_wait carries a suspend-time hint (in
+// ns), so a waiting warp sleeps until the phase completes instead of spinning
+// on issue slots that the warps sharing its scheduler need; the hint is far
+// below the overall budget.  A shorter budget (a diagnostic setting, see
+// tsd_set_wait_budget) takes a separate loop that polls with the non-blocking
+// test_wait, so the wait gives up as soon as the budget is spent; the choice
+// is made once per call, outside the loops (a test inside the sleeping loop
+// cost 10% of the attention kernel's time).
 constexpr uint32_t kSuspendHintNs = 1000000u;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity, long long budget) {
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > budget) return false;
+  }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          long long budget = kWaitCycles) {
+  if (budget < kWaitCycles) return mbar_poll(bar, parity, budget);
   const long long t0 = clock64();
   for (;;) {
     uint32_t ok;

@@ -178,6 +178,8 @@ verify_generic_kernel(const __grid_constant__ VerifyArgs a) {
 // tests use it to check every path against the oracle); the default is the
 // automatic choice below.
 static std::atomic<int> g_forced_path{TSD_PATH_AUTO};
+// Budget of the tcgen05 kernels' pipeline waits, in clock cycles (0 = default).
+static std::atomic<long long> g_wait_budget{0};
 
 static int choose_path(const tsd_attn_desc& d, int M) {
   const bool gqa_bf16 = d.dtype == TSD_BF16 && !d.v_aliases_k && d.dk == d.dv;
@@ -305,6 +307,10 @@ static bool desc_ok(const tsd_attn_desc* d) {
   return mla || gqa;
 }
 
+extern "C" long long tsd_set_wait_budget(long long cycles) {
+  return g_wait_budget.exchange(cycles > 0 ? cycles : 0);
+}
+
 extern "C" int tsd_set_verify_path(int path) {
   if (path < TSD_PATH_AUTO || path > TSD_PATH_TCGEN05) return -1;
   return g_forced_path.exchange(path);
@@ -348,6 +354,10 @@ static tsd_status verify_impl(const tsd_attn_desc* d, const void* q, const void*
   a.nsplit = p.nsplit; a.split_len = p.split_len; a.nrg = p.nrg;
   a.qscale = d->scale * 1.4426950408889634f;
   a.err = err;
+  {
+    const long long wb = g_wait_budget.load(std::memory_order_relaxed);
+    a.wait_cycles = wb > 0 && wb < kWaitCycles ? wb : kWaitCycles;
+  }
   a.page_table = paged ? page_table : nullptr;
   a.max_pages = paged ? max_pages : 0;
   a.page_size = paged ? page_size : 0;

@@ -26,6 +26,7 @@ struct VerifyArgs {
   float* ws_o;    // [B][Hq][R][nsplit][dv] normalised partial outputs
   float* ws_lse;  // [B][Hq][R][nsplit] log2-sum-exp of each partial
   int32_t* err;
+  long long wait_cycles;   // budget of the tcgen05 kernels' pipeline waits (clock cycles)
   int B, R, Hq, Hkv, g, M, cap;
   int nsplit, split_len, nrg;
   float qscale;   // softmax scale * log2(e): scores are kept in the log2 domain

@@ -46,9 +46,11 @@
 // 2^(m_old - m_new) before phase 2.  Row sums are reduced across lanes once,
 // at the end.
 //
-// Every mbarrier wait is bounded (about a second); a timeout sets
-// TSD_DEV_ERR_TIMEOUT in the error word, all roles stop, in-flight copies and
-// MMAs are waited for (again bounded) and the tensor memory is released.
+// Every mbarrier wait is bounded; a timeout sets TSD_DEV_ERR_TIMEOUT in the
+// error word, all roles stop, in-flight copies and MMAs are waited for and the
+// tensor memory is released.  The pipeline waits take their budget from the
+// call (about a second by default, see tsd_set_wait_budget); the teardown
+// waits for copies and products in flight always keep the full budget.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -303,7 +305,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       for (int t = kKStages; t < kKStages + kPrefetch; ++t) prefetch(&maps.k, t);
       // K_t reuses the stage of tile t-3 once O^T_(t-3) has read its P^T
       for (int t = kKStages; t < ntiles && !flags[1]; ++t) {
-        if (!mbar_wait(bar(BAR_K_EMPTY + t % kKStages), (t / kKStages - 1) & 1)) {
+        if (!mbar_wait(bar(BAR_K_EMPTY + t % kKStages), (t / kKStages - 1) & 1, a.wait_cycles)) {
           flags[1] = 1;
           break;
         }
@@ -322,7 +324,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       int nv = 0;
       for (int t = 1; t < 1 + kPrefetch; ++t) prefetch(&maps.v, t);
       for (int tv = 0; tv < ntiles && !flags[1]; ++tv) {
-        if (tv >= 2 && !mbar_wait(bar(BAR_V_EMPTY + (tv & 1)), ((tv - 2) >> 1) & 1)) {
+        if (tv >= 2 && !mbar_wait(bar(BAR_V_EMPTY + (tv & 1)), ((tv - 2) >> 1) & 1, a.wait_cycles)) {
           flags[1] = 1;
           break;
         }
@@ -353,7 +355,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       const uint64_t ptd0 = smem_desc_interleave(sbase + L::off_k, 16 * N, 128);
       auto issue_qk = [&](int t) -> bool {
         const int stg = t % kKStages;
-        if (!mbar_wait(bar(BAR_K_FULL + stg), (t / kKStages) & 1)) return false;
+        if (!mbar_wait(bar(BAR_K_FULL + stg), (t / kKStages) & 1, a.wait_cycles)) return false;
         fence_after();
         const uint64_t kd = kd0 + (uint64_t)(stg * (L::stage >> 4));
         const uint32_t ts = tm_s[t & 1];
@@ -368,8 +370,8 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       bool ok = issue_qk(0);
       for (int t = 0; ok && t < ntiles; ++t) {
         if (t + 1 < ntiles && !issue_qk(t + 1)) { ok = false; break; }
-        if (!mbar_wait(bar(BAR_P_FULL + (t & 1)), (t >> 1) & 1) || flags[1]) { ok = false; break; }
-        if (!mbar_wait(bar(BAR_V_FULL + (t & 1)), (t >> 1) & 1)) { ok = false; break; }
+        if (!mbar_wait(bar(BAR_P_FULL + (t & 1)), (t >> 1) & 1, a.wait_cycles) || flags[1]) { ok = false; break; }
+        if (!mbar_wait(bar(BAR_V_FULL + (t & 1)), (t >> 1) & 1, a.wait_cycles)) { ok = false; break; }
         fence_after();
         const int stg = t % kKStages;
         const uint64_t vd = vd0 + (uint64_t)((t & 1) * (kTileBytes >> 4));
@@ -413,7 +415,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
     for (int t = 0; t < ntiles; ++t) {
       const int st = t & 1;
       // tcgen05.ld is warp-collective: the whole warp agrees on the wait
-      const bool ok = __all_sync(kFull, mbar_wait(bar(BAR_S_FULL + st), (t >> 1) & 1));
+      const bool ok = __all_sync(kFull, mbar_wait(bar(BAR_S_FULL + st), (t >> 1) & 1, a.wait_cycles));
       fence_after();
       const bool is_tree = t >= n_pre;
       const int nvalid = is_tree ? a.R : min(kKeys, k1 - (k0 + t * kKeys));
@@ -526,7 +528,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
           // the previous tile's O^T product must be complete before its
           // columns are rescaled in TMEM
           if (t > 0 && !pv_waited) {
-            if (!__all_sync(kFull, mbar_wait(bar(BAR_PV_DONE), (t - 1) & 1))) failed = true;
+            if (!__all_sync(kFull, mbar_wait(bar(BAR_PV_DONE), (t - 1) & 1, a.wait_cycles))) failed = true;
             fence_after();
             pv_waited = true;
           }
@@ -595,12 +597,15 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       // V rows of keys past the range may hold anything: zero them (the
       // warpgroup of the first columns does it)
       if (wg == 0 && key >= nvalid) {
-        if (!mbar_wait(bar(BAR_V_FULL + st), (t >> 1) & 1)) failed = true;
-        uint8_t* vrow = smem + L::off_v + st * kTileBytes + key * 128u;
+        if (!mbar_wait(bar(BAR_V_FULL + st), (t >> 1) & 1, a.wait_cycles)) {
+          failed = true;                     // the copy may still be landing: no writes
+        } else {
+          uint8_t* vrow = smem + L::off_v + st * kTileBytes + key * 128u;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          *(uint4*)(vrow + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-          *(uint4*)(vrow + kBox + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+          for (int i = 0; i < 8; ++i) {
+            *(uint4*)(vrow + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+            *(uint4*)(vrow + kBox + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -610,7 +615,9 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
     }
 
     // ---------------------------------------------------------- epilogue
-    bool ok = !failed && __all_sync(kFull, mbar_wait(bar(BAR_O_DONE), 0));
+    // (a failed V wait above is per lane: agree on it across the warp)
+    failed = __any_sync(kFull, failed);
+    const bool ok = !failed && __all_sync(kFull, mbar_wait(bar(BAR_O_DONE), 0, a.wait_cycles));
     fence_after();
     const bool stop = wg_bar_or(wg, !ok || flags[1] != 0);
     if (!stop) {
@@ -663,7 +670,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
         }
       }
     }
-    if (failed && lane == 0) flags[1] = 1;
+    if (!ok && lane == 0) flags[1] = 1;      // a failed wait of this warp's, or O_DONE's
   }
 
   // --------------------------------------------------------------- teardown
