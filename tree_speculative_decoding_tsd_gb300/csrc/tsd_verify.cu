@@ -220,19 +220,34 @@ VerifyPlan plan_verify(const tsd_attn_desc& d) {
     // packed rows on the MMA N dimension: at most 144 per CTA, multiple of 16
     p.nrg = (int)ceil_div(M, 144);
     p.rb = (int)ceil_div(ceil_div(M, p.nrg), 16) * 16;
-    // Splits: about two waves of CTAs for the whole batch.  A split writes a
-    // partial output as large as ~130 keys of K/V, so splits stay >= 256 keys
-    // (>= 1024 once the batch alone fills the GPU) and <= 4096 keys; for a
-    // small batch the shorter splits shorten the critical path (qwen-sized
-    // step: 256-key splits 2.5 us faster than 512).  The split depends on B:
-    // results are deterministic, but their rounding can differ between batch
-    // sizes.
+    // Splits.  A small batch takes about two waves of CTAs: splits of 256 to
+    // 4096 keys, the shorter ones shortening the critical path (qwen-sized
+    // step: 256-key splits 2.5 us faster than 512).  Once the batch has at
+    // least 64 (request, KV head, row group) units, the split count ns
+    // minimises the modelled time of full-length requests: waves of CTAs,
+    // ceil(units * ns / 152), times the tiles of one CTA plus its set-up and
+    // epilogue (about 4 tiles' worth).  For the batched workload (256 units of
+    // <= 33 tiles) that is no split at all -- every CTA writes its output and
+    // no merge runs -- and for long prefixes (128 units of 257 tiles) 7
+    // splits, 6 full waves.  The split depends on B: results are
+    // deterministic, but their rounding can differ between batch sizes.
     const long units = (long)d.B * d.Hkv * p.nrg;
-    ns = ceil_div(152L * 2, units);
-    long len = ceil_div(ceil_div(d.cap, ns), 128) * 128;  // whole 128-key tiles
-    const long lo = units >= 152 ? 1024 : 256;
-    if (len < lo) len = lo;
-    if (len > 4096) len = 4096;
+    const long tiles = ceil_div(d.cap, 128);
+    long len;
+    if (units >= 64) {
+      long best = -1, best_ns = 1;
+      for (long n = 1; n <= 32 && n <= tiles; ++n) {
+        const long per = ceil_div(tiles, n);
+        const long cost = ceil_div(units * n, 152L) * (per + 4);
+        if (best < 0 || cost < best) { best = cost; best_ns = n; }
+      }
+      len = ceil_div(tiles, best_ns) * 128;
+    } else {
+      ns = ceil_div(152L * 2, units);
+      len = ceil_div(ceil_div(d.cap, ns), 128) * 128;  // whole 128-key tiles
+      if (len < 256) len = 256;
+      if (len > 4096) len = 4096;
+    }
     p.split_len = (int)len;
   } else if (p.path == kPathMma) {
     // one warp per 16 packed rows, at most 8 warps per CTA, balanced groups

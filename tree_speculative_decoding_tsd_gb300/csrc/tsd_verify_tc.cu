@@ -64,8 +64,8 @@
 namespace tsd {
 namespace {
 
-constexpr int kKeys = 128;          // keys per tile (MMA M of S^T)
-constexpr int kD = 128;             // head dim
+constexpr int kKeys = 128;                      // keys per tile (MMA M of S^T)
+constexpr int kD = 128;                         // head dim
 constexpr int kSoftWarps = 16;                  // 4 warpgroups, one quarter of the columns each
 constexpr int kThreadsTC = (kSoftWarps + 3) * 32;
 constexpr int kMmaWarp = 16, kTmaWarp = 17, kTmaVWarp = 18;
@@ -74,7 +74,11 @@ constexpr uint32_t kTileBytes = 2 * kBox;       // one K or V tile: 32 KB
 constexpr int kKStages = 3;                     // K ring (each stage then holds that tile's P^T)
 constexpr int kPagedTiles = 64;  // paged cache: tile rows resolved at set-up
 constexpr float kOverflow = 8.0f;               // log2 headroom of the lazy max
-constexpr int kPrefetch = 3;                    // prefix tiles prefetched into L2 ahead
+// Prefix tiles prefetched into L2 ahead of their shared-memory load.  One is
+// best measured (batched workload: 1 tile 125 us, 3 tiles 128, 5 tiles 136):
+// deeper prefetches only compete with the loads for L2 and DRAM.
+constexpr int kPrefetch = 1;
+constexpr int kLptMaxBatch = 64;                // longest-first request order up to this batch
 
 template <int N>
 struct TcLayout {
@@ -101,7 +105,7 @@ struct TcLayout {
   static constexpr uint32_t off_ooff = off_rmask + 8 * N;           // i64[N] output offsets
   static constexpr uint32_t off_bar = off_ooff + 8 * N;             // mbarriers
   static constexpr int nbar = 17;
-  static constexpr uint32_t off_flags = off_bar + 8 * nbar;          // tmem addr, abort flag
+  static constexpr uint32_t off_flags = off_bar + 8 * nbar;  // tmem addr, abort flag, request
   static constexpr uint32_t off_tiles = off_flags + 16;  // int[kPagedTiles] tile rows (paged)
   static constexpr uint32_t total = off_tiles + 4 * kPagedTiles;
   static_assert(total + 1024 <= 232448, "shared memory budget");
@@ -138,10 +142,15 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
     tma_desc_prefetch(&maps.kt);
     tma_desc_prefetch(&maps.vt);
   }
+  // Requests are taken longest first when the batch has 2 to 64 of them
+  // (grid z is the rank of the request in (prefix length desc, index asc)
+  // order), so that the last wave holds the shortest CTAs.
+  const bool lpt = a.B > 1 && a.B <= kLptMaxBatch;
   // While the previous kernel finishes: L2 prefetch of this CTA's first two
   // prefix tiles (K and V, one warp each; contiguous cache only, the page
-  // table may still be being written) and of its Q rows.  Hints only.
-  {
+  // table may still be being written) and of its Q rows.  Hints only, and
+  // only where the request is known before the prefix lengths are read.
+  if (!lpt) {
     const int w = threadIdx.x >> 5, ln = threadIdx.x & 31;
     const int hk0 = blockIdx.y / a.nrg, b0 = blockIdx.z;
     const int kp0 = blockIdx.x * a.split_len;
@@ -178,14 +187,33 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
   float* shiftv = (float*)(smem + L::off_shift);
   uint64_t* rmask = (uint64_t*)(smem + L::off_rmask);
   long long* ooff = (long long*)(smem + L::off_ooff);
-  volatile uint32_t* flags = (volatile uint32_t*)(smem + L::off_flags);  // [0] tmem, [1] abort
+  volatile uint32_t* flags = (volatile uint32_t*)(smem + L::off_flags);  // [0] tmem, [1] abort, [2] b
   const uint32_t bar0 = sbase + L::off_bar;
   auto bar = [&](int i) { return bar0 + 8u * i; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sp = blockIdx.x;
   const int hk = blockIdx.y / a.nrg, rg = blockIdx.y % a.nrg;
-  const int b = blockIdx.z;
+  int b = blockIdx.z;
+  if (lpt) {
+    // warp 0 ranks the requests (lane l holds requests l and l + 32); the one
+    // of rank blockIdx.z is this CTA's
+    if (warp == 0) {
+      const int i0 = lane, i1 = lane + 32;
+      const int p0 = i0 < a.B ? min(max(a.plen[i0], 0), a.cap) : -1;
+      const int p1 = i1 < a.B ? min(max(a.plen[i1], 0), a.cap) : -1;
+      int r0 = 0, r1 = 0;
+      for (int j = 0; j < a.B; ++j) {
+        const int pj = __shfl_sync(kFull, j < 32 ? p0 : p1, j & 31);
+        r0 += (pj > p0 || (pj == p0 && j < i0)) ? 1 : 0;
+        r1 += (pj > p1 || (pj == p1 && j < i1)) ? 1 : 0;
+      }
+      if (i0 < a.B && r0 == (int)blockIdx.z) flags[2] = (uint32_t)i0;
+      if (i1 < a.B && r1 == (int)blockIdx.z) flags[2] = (uint32_t)i1;
+    }
+    __syncthreads();
+    b = (int)flags[2];
+  }
   const int P = min(max(a.plen[b], 0), a.cap);
   const int nsb = P > 0 ? (P + a.split_len - 1) / a.split_len : 1;
   if (sp >= nsb) return;  // uniform for the whole CTA, before any barrier or allocation
