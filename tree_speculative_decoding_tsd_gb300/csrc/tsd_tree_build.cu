@@ -37,6 +37,12 @@ struct TreeSmem {
   float tp[kMaxS][kMaxK];     // top-k probabilities per position
   int32_t ti[kMaxS][kMaxK];   // top-k token ids per position
   float cost[kMaxD + 1];      // adaptive mode: C_d + C_v(n), n = 0..D
+  // the tree's rows, written by lane 0 as they are popped
+  uint64_t r_mask[kMaxD + 1];
+  float r_sc[kMaxD + 1];
+  int32_t r_par[kMaxD + 1];
+  int32_t r_tok[kMaxD + 1];
+  int32_t r_dep[kMaxD + 1];
   uint8_t has_child[kMaxD + 1];
 };
 
@@ -47,13 +53,14 @@ __device__ __forceinline__ void tuple_add(uint64_t& w0, uint64_t& w1, int level,
   else w1 += digit << (59 - 5 * (level - 12));
 }
 
-// Primary key of a frontier entry: score descending (the bit pattern of a
-// non-negative float grows with it), then depth, then the first 27 tuple bits.
-// Entries with different keys are ordered by the key alone; equal keys (equal
-// score and depth, same leading ranks) are resolved by the full comparison.
-__device__ __forceinline__ uint64_t primary_key(float sc, int depth, uint64_t w0) {
-  return ((uint64_t)(~__float_as_uint(sc)) << 32) | ((uint64_t)depth << 27) | (w0 >> 37);
-}
+// Primary key of a frontier entry: the score's bit pattern inverted (the bit
+// pattern of a non-negative float grows with it), so the smallest key is the
+// highest score.  Entries with different keys are ordered by the key alone;
+// equal keys (equal scores) are resolved by the full comparison.
+__device__ __forceinline__ uint32_t score_key(float sc) { return ~__float_as_uint(sc); }
+
+// Depth, parent row and rank of a frontier entry in one word (each < 256).
+__device__ __forceinline__ int pack_dpr(int d, int par, int rk) { return d | (par << 8) | (rk << 16); }
 
 // Full order between two frontier entries (score desc, depth asc, tuple asc).
 __device__ __forceinline__ bool precedes(float sa, int da, uint64_t a0, uint64_t a1, float sb,
@@ -64,11 +71,10 @@ __device__ __forceinline__ bool precedes(float sa, int da, uint64_t a0, uint64_t
   return a1 < b1;
 }
 
-// Per-lane register slots: frontier entry / row e lives in lane e % 32, slot
-// e / 32.  The frontier never holds more than D + 1 entries and there are D + 1
-// rows, so ceil((D + 2) / 32) slots suffice; the kernel is instantiated for
-// 1, 2 and 3 slots (D <= 30, 62, 64) because every pick and put costs one
-// select per slot.
+// Per-lane register slots: frontier entry e lives in lane e % 32, slot e / 32.
+// The frontier never holds more than D + 1 entries, so ceil((D + 2) / 32)
+// slots suffice; the kernel is instantiated for 1, 2 and 3 slots (D <= 30,
+// 62, 64) because every pick and put costs one select per slot.
 template <int NS, typename T>
 __device__ __forceinline__ T pick(const T (&v)[NS], int j) {
   T r = v[0];
@@ -87,7 +93,7 @@ __device__ __forceinline__ T bcast(const T (&v)[NS], int e) {
 }
 
 template <int kSlots>
-__global__ void __launch_bounds__(32 * kMaxS)
+__global__ void __launch_bounds__(32 * kMaxS, 1)
 best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, int nchunk,
                        const int32_t* __restrict__ root_tok, int32_t* __restrict__ token,
                        int32_t* __restrict__ parent, int32_t* __restrict__ depth,
@@ -128,24 +134,26 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   __syncthreads();
   if (warp != 0) return;
 
-  // ---- frontier and rows in registers, spread over the lanes ----
+  // ---- frontier in registers, spread over the lanes; rows in shared memory ----
   // A frontier entry also carries its parent's score and ancestor mask, so a
-  // pop needs no lookup of the parent row.
-  float f_sc[kSlots], f_psc[kSlots], r_sc[kSlots];
-  int32_t f_d[kSlots], f_par[kSlots], f_rk[kSlots], r_par[kSlots], r_tok[kSlots], r_dep[kSlots];
-  uint64_t f_w0[kSlots], f_w1[kSlots], f_key[kSlots], f_pm[kSlots], r_mask[kSlots];
+  // pop needs no lookup of the parent row.  Lane 0 writes each popped row to
+  // shared memory (no per-lane selects on the critical path).
+  float f_sc[kSlots], f_psc[kSlots];
+  uint32_t f_key[kSlots];
+  int32_t f_dpr[kSlots];
+  uint64_t f_w0[kSlots], f_w1[kSlots], f_pm[kSlots];
 #pragma unroll
   for (int j = 0; j < kSlots; ++j) {
-    f_sc[j] = 0.f; f_psc[j] = 0.f; f_d[j] = 0; f_par[j] = 0; f_rk[j] = 0;
-    f_w0[j] = 0ull; f_w1[j] = 0ull; f_key[j] = ~0ull; f_pm[j] = 0ull;
-    r_sc[j] = 0.f; r_par[j] = 0; r_tok[j] = 0; r_dep[j] = 0; r_mask[j] = 0ull;
+    f_sc[j] = 0.f; f_psc[j] = 0.f; f_key[j] = ~0u; f_dpr[j] = 0;
+    f_w0[j] = 0ull; f_w1[j] = 0ull; f_pm[j] = 0ull;
   }
   // row 0 = root; frontier slot 0 = rank 0 at depth 1
   if (lane == 0) {
-    r_sc[0] = 1.0f; r_par[0] = -1; r_tok[0] = root_tok[b]; r_dep[0] = 0; r_mask[0] = 0ull;
-    f_sc[0] = __fmul_rn(1.0f, s.tp[0][0]); f_psc[0] = 1.0f; f_d[0] = 1; f_par[0] = 0;
-    f_rk[0] = 0; f_pm[0] = 0ull;
-    f_key[0] = primary_key(f_sc[0], 1, 0ull);
+    s.r_sc[0] = 1.0f; s.r_par[0] = -1; s.r_tok[0] = root_tok[b]; s.r_dep[0] = 0;
+    s.r_mask[0] = 0ull;
+    f_sc[0] = __fmul_rn(1.0f, s.tp[0][0]); f_psc[0] = 1.0f; f_dpr[0] = pack_dpr(1, 0, 0);
+    f_pm[0] = 0ull;
+    f_key[0] = score_key(f_sc[0]);
   }
   int nf = 1;
   // Phi accumulation for the adaptive stop: A = 1 + Phi(first n nodes), fp32
@@ -155,36 +163,35 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   int kept = D;
 
   for (int row = 1; row <= D; ++row) {
-    // this lane's smallest primary key, then the warp's: high word (score),
-    // then low word (depth, leading ranks) among the lanes that hold the high
-    uint64_t kmin = ~0ull;
+    // this lane's smallest key, then the warp's; one holder of one entry is
+    // the common case, several entries with the key (equal scores) take the
+    // full comparison
+    uint32_t kmin = ~0u;
     int mine = -1;
 #pragma unroll
     for (int j = 0; j < kSlots; ++j) {
       const int e = lane + 32 * j;
-      if (e < nf && f_key[j] < kmin) { kmin = f_key[j]; mine = e; }
+      // (a score of 0 has the key ~0u, so "no entry yet" is mine < 0)
+      if (e < nf && (mine < 0 || f_key[j] < kmin)) { kmin = f_key[j]; mine = e; }
     }
-    const unsigned hi = (unsigned)(kmin >> 32), lo = (unsigned)kmin;
-    const unsigned hmin = __reduce_min_sync(kFull, hi);
-    const unsigned lmin = __reduce_min_sync(kFull, hi == hmin ? lo : 0xffffffffu);
-    const bool holder = mine >= 0 && hi == hmin && lo == lmin;
-    const unsigned hb = __ballot_sync(kFull, holder);
+    const uint32_t hmin = __reduce_min_sync(kFull, kmin);
     int ties = 0;
 #pragma unroll
-    for (int j = 0; j < kSlots; ++j)
-      ties += (lane + 32 * j < nf && f_key[j] == ((uint64_t)hmin << 32 | lmin)) ? 1 : 0;
+    for (int j = 0; j < kSlots; ++j) ties += (lane + 32 * j < nf && f_key[j] == hmin) ? 1 : 0;
+    const unsigned hb = __ballot_sync(kFull, ties > 0);
+    const unsigned hm = __ballot_sync(kFull, ties > 1);
     int best = __shfl_sync(kFull, mine, __ffs(hb) - 1);
-    if (__popc(hb) > 1 || __any_sync(kFull, ties > 1)) {
-      // equal primary keys (equal score, depth and leading ranks): full order
-      const uint64_t kk = (uint64_t)hmin << 32 | lmin;
+    if (__popc(hb) > 1 || hm != 0u) {
+      // equal scores: full order (depth, then rank tuple)
       int b2 = -1;
       float bs = 0.f; int bd = 0; uint64_t b0 = 0ull, b1 = 0ull;
 #pragma unroll
       for (int j = 0; j < kSlots; ++j) {
         const int e = lane + 32 * j;
-        if (e < nf && f_key[j] == kk &&
-            (b2 < 0 || precedes(f_sc[j], f_d[j], f_w0[j], f_w1[j], bs, bd, b0, b1))) {
-          b2 = e; bs = f_sc[j]; bd = f_d[j]; b0 = f_w0[j]; b1 = f_w1[j];
+        const int dj = f_dpr[j] & 0xff;
+        if (e < nf && f_key[j] == hmin &&
+            (b2 < 0 || precedes(f_sc[j], dj, f_w0[j], f_w1[j], bs, bd, b0, b1))) {
+          b2 = e; bs = f_sc[j]; bd = dj; b0 = f_w0[j]; b1 = f_w1[j];
         }
       }
 #pragma unroll
@@ -209,17 +216,18 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       }
       acc = acc1;
     }
-    const int d = bcast<kSlots>(f_d, best), par = bcast<kSlots>(f_par, best);
-    const int rk = bcast<kSlots>(f_rk, best);
+    const int dpr = bcast<kSlots>(f_dpr, best);
+    const int d = dpr & 0xff, par = (dpr >> 8) & 0xff, rk = dpr >> 16;
     const uint64_t w0 = bcast<kSlots>(f_w0, best), w1 = bcast<kSlots>(f_w1, best);
     const uint64_t pm = bcast<kSlots>(f_pm, best);
     const uint64_t m = pm | (1ull << (row - 1));
-    const int rl = row & 31, rj = row >> 5;
-    put<kSlots>(r_sc, rj, sc, lane == rl);
-    put<kSlots>(r_par, rj, par, lane == rl);
-    put<kSlots>(r_tok, rj, s.ti[d - 1][rk], lane == rl);
-    put<kSlots>(r_dep, rj, d, lane == rl);
-    put<kSlots>(r_mask, rj, m, lane == rl);
+    if (lane == 0) {
+      s.r_sc[row] = sc;
+      s.r_par[row] = par;
+      s.r_tok[row] = s.ti[d - 1][rk];
+      s.r_dep[row] = d;
+      s.r_mask[row] = m;
+    }
     // the popped slot becomes the next sibling, or takes the last entry
     const int bl = best & 31, bj = best >> 5;
     const int last = nf - 1;
@@ -228,19 +236,18 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       uint64_t nw0 = w0, nw1 = w1;
       tuple_add(nw0, nw1, d - 1, 1ull);
       const bool me = lane == bl;
-      put<kSlots>(f_sc, bj, nsc, me); put<kSlots>(f_rk, bj, rk + 1, me);
+      put<kSlots>(f_sc, bj, nsc, me); put<kSlots>(f_dpr, bj, pack_dpr(d, par, rk + 1), me);
       put<kSlots>(f_w0, bj, nw0, me); put<kSlots>(f_w1, bj, nw1, me);
-      put<kSlots>(f_key, bj, primary_key(nsc, d, nw0), me);
+      put<kSlots>(f_key, bj, score_key(nsc), me);
     } else {
       const float lsc = bcast<kSlots>(f_sc, last), lps = bcast<kSlots>(f_psc, last);
-      const int ld = bcast<kSlots>(f_d, last), lp = bcast<kSlots>(f_par, last);
-      const int lr = bcast<kSlots>(f_rk, last);
+      const int ldpr = bcast<kSlots>(f_dpr, last);
       const uint64_t l0 = bcast<kSlots>(f_w0, last), l1 = bcast<kSlots>(f_w1, last);
-      const uint64_t lk = bcast<kSlots>(f_key, last);
+      const uint32_t lk = bcast<kSlots>(f_key, last);
       const uint64_t lm = bcast<kSlots>(f_pm, last);
       const bool me = lane == bl;
-      put<kSlots>(f_sc, bj, lsc, me); put<kSlots>(f_psc, bj, lps, me); put<kSlots>(f_d, bj, ld, me);
-      put<kSlots>(f_par, bj, lp, me); put<kSlots>(f_rk, bj, lr, me); put<kSlots>(f_w0, bj, l0, me);
+      put<kSlots>(f_sc, bj, lsc, me); put<kSlots>(f_psc, bj, lps, me);
+      put<kSlots>(f_dpr, bj, ldpr, me); put<kSlots>(f_w0, bj, l0, me);
       put<kSlots>(f_w1, bj, l1, me); put<kSlots>(f_key, bj, lk, me); put<kSlots>(f_pm, bj, lm, me);
       nf = last;
     }
@@ -250,13 +257,14 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       const bool me = lane == (nf & 31);
       const int cj = nf >> 5;
       put<kSlots>(f_sc, cj, csc, me); put<kSlots>(f_psc, cj, sc, me);
-      put<kSlots>(f_d, cj, d + 1, me);
-      put<kSlots>(f_par, cj, row, me); put<kSlots>(f_rk, cj, 0, me); put<kSlots>(f_w0, cj, w0, me);
+      put<kSlots>(f_dpr, cj, pack_dpr(d + 1, row, 0), me);
+      put<kSlots>(f_w0, cj, w0, me);
       put<kSlots>(f_w1, cj, w1, me); put<kSlots>(f_pm, cj, m, me);
-      put<kSlots>(f_key, cj, primary_key(csc, d + 1, w0), me);
+      put<kSlots>(f_key, cj, score_key(csc), me);
       ++nf;
     }
   }
+  __syncwarp();
 
   // ---- leaves and outputs (each lane writes its own rows) ----
   // Rows past the kept count (adaptive mode only) are inert padding: token -1
@@ -264,23 +272,17 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   // leaf, so verify, walk and commit treat them as never accepted.
   for (int r = lane; r <= D; r += 32) s.has_child[r] = 0;
   __syncwarp();
-#pragma unroll
-  for (int j = 0; j < kSlots; ++j) {
-    const int r = lane + 32 * j;
-    if (r >= 1 && r <= kept) s.has_child[r_par[j]] = 1;
-  }
+  for (int r = 1 + lane; r <= kept; r += 32) s.has_child[s.r_par[r]] = 1;
   __syncwarp();
-#pragma unroll
-  for (int j = 0; j < kSlots; ++j) {
-    const int r = lane + 32 * j;
+  for (int r = lane; r <= D; r += 32) {
     if (r <= kept) {
-      token[o + r] = r_tok[j];
-      parent[o + r] = r_par[j];
-      depth[o + r] = r_dep[j];
-      score[o + r] = r_sc[j];
-      mask[o + r] = r_mask[j];
+      token[o + r] = s.r_tok[r];
+      parent[o + r] = s.r_par[r];
+      depth[o + r] = s.r_dep[r];
+      score[o + r] = s.r_sc[r];
+      mask[o + r] = s.r_mask[r];
       is_leaf[o + r] = s.has_child[r] ? 0 : 1;
-    } else if (r <= D) {
+    } else {
       token[o + r] = -1;
       parent[o + r] = 0;
       depth[o + r] = 0;
