@@ -33,7 +33,12 @@
 // N/16 is odd, the quad 32(N/32) + 4w .. +3), so its P^T rows are 16-byte
 // (or 8-byte) stores at per-thread offsets fixed for the whole kernel.  P^T is
 // kept MN-major without swizzle: 8x8 core matrices of 128 contiguous bytes,
-// cores along N adjacent (128 B apart), groups of 8 keys N/8 cores apart.
+// the 16 groups of 8 keys of one 8-column core column adjacent (128 B apart),
+// core columns 2 KB apart, so the 32 keys of a warp store 512 contiguous
+// bytes and the 16 keys of one K step of the O^T product are 256 contiguous
+// bytes per core column.  (With the groups of 8 keys N/8 cores apart the
+// long workload's verify took 2% longer; ncu counts the same shared-memory
+// store wavefronts for both layouts.)
 //
 // Softmax with keys on lanes: a thread holds one key's scores for its
 // columns, so a column's max and sum are cross-lane reductions, and the
@@ -375,12 +380,13 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       const uint32_t idesc_pv = idesc_qk | (1u << 15) | (1u << 16);
       // descriptor bases (built once): K stage 0, V stage 0, Q^T, and P^T in
       // K stage 0 (MN-major without swizzle, where the leading offset is the
-      // stride between groups of 8 keys, 16N B, and the stride offset the one
-      // between cores along N, 128 B)
+      // stride between groups of 8 keys, 128 B, and the stride offset the one
+      // between cores along N, 2 KB: the 16 key groups of 8 columns are one
+      // contiguous 2 KB block, so a warp's 32 keys store 512 contiguous bytes)
       const uint64_t kd0 = smem_desc(sbase + L::off_k, 16, 1024);
       const uint64_t vd0 = smem_desc(sbase + L::off_v, kBox, 1024);
       const uint64_t qd0 = smem_desc(sbase + L::off_q, 16, 1024);
-      const uint64_t ptd0 = smem_desc_interleave(sbase + L::off_k, 16 * N, 128);
+      const uint64_t ptd0 = smem_desc_interleave(sbase + L::off_k, 128, 2048);
       auto issue_qk = [&](int t) -> bool {
         const int stg = t % kKStages;
         if (!mbar_wait(bar(BAR_K_FULL + stg), (t / kKStages) & 1, a.wait_cycles)) return false;
@@ -408,7 +414,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
         else mma_f16_acc(tm_o, vd, pd, idesc_pv);
 #pragma unroll
         for (int kk = 1; kk < kKeys / 16; ++kk)
-          mma_f16_acc(tm_o, vd + 128 * kk, pd + (uint64_t)(2 * N * kk), idesc_pv);
+          mma_f16_acc(tm_o, vd + 128 * kk, pd + (uint64_t)(16 * kk), idesc_pv);
         mma_commit(bar(BAR_PV_DONE));
         mma_commit(bar(BAR_V_EMPTY + (t & 1)));
         mma_commit(bar(BAR_K_EMPTY + stg));
@@ -427,11 +433,11 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
     const int wg = warp >> 2, q = warp & 3;
     const int key = q * 32 + lane;           // TMEM lane = key of the tile / dim of O^T
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    // P^T row of this key: octet u at pt_oct + 512u, the quad at pt_quad
-    // (offsets within a K stage)
-    const uint32_t pt_key = (uint32_t)(key >> 3) * (16u * N) + (uint32_t)(key & 7) * 16u;
-    const uint32_t pt_oct = pt_key + (uint32_t)wg * 128u;
-    const uint32_t pt_quad = pt_key + (4u * NO + (uint32_t)(wg >> 1)) * 128u + (uint32_t)(wg & 1) * 8u;
+    // P^T row of this key: octet u at pt_oct + 8192u (columns 32u + 8wg..+7,
+    // core column 4u + wg), the quad at pt_quad (offsets within a K stage)
+    const uint32_t pt_key = (uint32_t)key * 16u;
+    const uint32_t pt_oct = pt_key + (uint32_t)wg * 2048u;
+    const uint32_t pt_quad = pt_key + (4u * NO + (uint32_t)(wg >> 1)) * 2048u + (uint32_t)(wg & 1) * 8u;
     // first S^T / O^T column (and per-column smem slot) of octet 0 and of the quad
     const int c_oct = 8 * wg, c_quad = 32 * NO + 4 * wg;
     const float2 c2 = make_float2(a.qscale, a.qscale);
@@ -610,7 +616,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
           if (u < NO) {
             l2[li + 2] = __fadd2_rn(l2[li + 2], make_float2(p[4], p[5]));
             l2[li + 3] = __fadd2_rn(l2[li + 3], make_float2(p[6], p[7]));
-            *(uint4*)(pt_stage + pt_oct + 512u * u) =
+            *(uint4*)(pt_stage + pt_oct + 8192u * u) =
                 make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
                            pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
           } else {
