@@ -204,6 +204,24 @@ def test_verify_attention_empty_and_tiny_prefixes():
     check_attention(w, q, kc, vc, plen, kt, vt, d["tree"]["mask"])
 
 
+@pytest.mark.parametrize("B", [64, 65])
+def test_verify_large_batch_longest_first_order(B):
+    """Batches of 64 and more (request, KV head) units take the wave-cost split
+    rule; up to 64 requests the CTAs take requests longest first (warp 0 ranks
+    the prefix lengths, ties by index), 65 keeps the natural order.  Prefix
+    lengths mix zero, ties and a ragged tail; every row checked."""
+    over = dict(B=B, D=3, k=4, P=600, P_min=0, V=500)
+    d = inputs("batched", **over)
+    w = d["w"]
+    q, kc, vc, _, kt, vt = attn_inputs(w)
+    g = torch.Generator().manual_seed(B)
+    plen = torch.randint(0, 601, (B,), generator=g).int()
+    plen[::7] = 300                               # ties
+    plen[3] = 0
+    plen[5] = 600
+    check_attention(w, q, kc, vc, plen, kt, vt, d["tree"]["mask"])
+
+
 def test_verify_branch_isolation_bit_exact():
     """Changing scratch K/V of rows outside a node's ancestor path leaves the
     node's output bit-identical (research gap item 1 of the V4 review)."""
