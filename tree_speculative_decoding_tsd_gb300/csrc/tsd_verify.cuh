@@ -129,6 +129,40 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, int b, int r, 
                                              int lane) {
   const long row = ((long)b * a.R + r) * a.Hq + h;
   const long base = (((long)b * a.Hq + h) * a.R + r) * a.nsplit;
+  constexpr int NV = DV / 32;
+  constexpr int kB = NV > 4 ? 4 : 8;
+  // A row of at most kB splits (the common case) has its partials' loads
+  // issued together with the log-sum-exp loads, before the weights are known:
+  // one memory round trip instead of two.
+  if (nsb <= kB) {
+    float x[kB][NV];
+#pragma unroll
+    for (int u = 0; u < kB; ++u)
+#pragma unroll
+      for (int t = 0; t < NV; ++t)
+        x[u][t] = u < nsb ? a.ws_o[(base + u) * DV + lane + 32 * t] : 0.f;
+    const float l = lane < nsb ? a.ws_lse[base + lane] : -INFINITY;
+    float mx = l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    const float tot = mx + log2f(warp_sum(lane < nsb ? exp2f(l - mx) : 0.f));
+    const float wl = lane < nsb ? exp2f(l - tot) : 0.f;
+    float acc[NV];
+#pragma unroll
+    for (int t = 0; t < NV; ++t) acc[t] = 0.f;
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const float w = __shfl_sync(kFull, wl, u);
+      if (u < nsb) {
+#pragma unroll
+        for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, x[u][t], acc[t]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < NV; ++t) ((T*)a.out)[row * DV + lane + 32 * t] = cvt_out<T>(acc[t]);
+    if (lane == 0) a.lse[row] = tot * 0.69314718055994531f;
+    return;
+  }
   // L = log2 sum_s 2^(L_s): maximum, then per-lane partial sums (split s on
   // lane s % 32, in increasing s) reduced across the warp
   const float l0 = lane < nsb ? a.ws_lse[base + lane] : -INFINITY;
@@ -140,14 +174,12 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, int b, int r, 
   for (int s = lane + 32; s < nsb; s += 32) sum += exp2f(a.ws_lse[base + s] - mx);
   sum = warp_sum(sum);
   const float tot = mx + log2f(sum);
-  constexpr int NV = DV / 32;
   float acc[NV];
 #pragma unroll
   for (int t = 0; t < NV; ++t) acc[t] = 0.f;
   // acc = sum over s in increasing order of fma(w_s, O_s, acc); lane j of a
   // round of 32 splits holds w_(s0+j).  Batches of kB partials have their
   // loads in flight together; the rest is one predicated batch of kB or kB/2
-  constexpr int kB = NV > 4 ? 4 : 8;
   for (int s0 = 0; s0 < nsb; s0 += 32) {
     const int n = min(32, nsb - s0);
     const float wl = lane >= n ? 0.f : exp2f((s0 == 0 ? l0 : a.ws_lse[base + s0 + lane]) - tot);
