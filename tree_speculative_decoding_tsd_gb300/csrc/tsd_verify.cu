@@ -268,7 +268,14 @@ VerifyPlan plan_verify(const tsd_attn_desc& d) {
     p.split_len = (int)ceil_div(d.cap, ns);
   }
   p.nsplit = (int)ceil_div(d.cap, p.split_len);
-  p.ws_bytes = p.nsplit > 1 ? (size_t)d.B * d.Hq * d.R * p.nsplit * (d.dv + 1) * sizeof(float) : 0;
+  // The tcgen05 path of bf16 heads stores its split partials in bf16 (the
+  // normalised partial output of a split is a convex combination of bf16
+  // values; the merge weights stay fp32), halving the partials' traffic.
+  p.part_bf16 = (p.path == kPathTc && !d.v_aliases_k) ? 1 : 0;
+  const size_t pe = p.part_bf16 ? sizeof(__nv_bfloat16) : sizeof(float);
+  p.ws_bytes = p.nsplit > 1
+                   ? (size_t)d.B * d.Hq * d.R * p.nsplit * (d.dv * pe + sizeof(float))
+                   : 0;
   return p;
 }
 
@@ -362,8 +369,14 @@ static tsd_status verify_impl(const tsd_attn_desc* d, const void* q, const void*
   a.q = q; a.kc = kcache; a.vc = vcache; a.plen = prefix_len;
   a.kt = ktree; a.vt = vtree; a.mask = mask;
   a.out = out; a.lse = lse;
-  a.ws_o = (float*)ws;
-  a.ws_lse = p.nsplit > 1 ? (float*)ws + (size_t)d->B * d->Hq * d->R * p.nsplit * d->dv : nullptr;
+  {
+    const size_t nparts = (size_t)d->B * d->Hq * d->R * p.nsplit;
+    a.ws_o = p.part_bf16 ? nullptr : (float*)ws;
+    a.ws_ob = p.part_bf16 ? (__nv_bfloat16*)ws : nullptr;
+    a.ws_lse = p.nsplit > 1 ? (float*)((char*)ws + nparts * d->dv *
+                                                     (p.part_bf16 ? sizeof(__nv_bfloat16) : sizeof(float)))
+                            : nullptr;
+  }
   a.B = d->B; a.R = d->R; a.Hq = d->Hq; a.Hkv = d->Hkv; a.g = d->Hq / d->Hkv;
   a.M = d->R * a.g; a.cap = d->cap;
   a.nsplit = p.nsplit; a.split_len = p.split_len; a.nrg = p.nrg;

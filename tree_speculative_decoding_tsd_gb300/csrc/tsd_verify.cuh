@@ -23,7 +23,8 @@ struct VerifyArgs {
   const uint64_t* mask;
   void* out;
   float* lse;
-  float* ws_o;    // [B][Hq][R][nsplit][dv] normalised partial outputs
+  float* ws_o;    // [B][Hq][R][nsplit][dv] normalised partial outputs (fp32), or
+  __nv_bfloat16* ws_ob;  // the same in bf16 (tcgen05 path of bf16 heads); one of the two is set
   float* ws_lse;  // [B][Hq][R][nsplit] log2-sum-exp of each partial
   int32_t* err;
   long long wait_cycles;   // budget of the tcgen05 kernels' pipeline waits (clock cycles)
@@ -44,6 +45,7 @@ struct VerifyPlan {
   int nrg;        // row groups per KV head
   int nsplit;     // prefix splits (grid x); a request uses ceil(P / split_len)
   int split_len;
+  int part_bf16;  // split partials stored in bf16 (1) or fp32 (0)
   size_t ws_bytes;
 };
 
@@ -103,14 +105,18 @@ __device__ __forceinline__ float warp_sum(float v) {
 // acc += w_(j+u) * O_(j+u) for u < m (m <= U, in increasing u), lane-strided
 // partials of DV = 32 * NV values at src[(j + u) * DV + 32 * t]; the weights
 // sit on lanes j..j+m-1 of wl.  All loads are issued before the products.
-template <int U, int NV>
-__device__ __forceinline__ void merge_batch(float (&acc)[NV], const float* src, float wl, int j,
+__device__ __forceinline__ float part_f32(float x) { return x; }
+__device__ __forceinline__ float part_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <int U, int NV, typename PT>
+__device__ __forceinline__ void merge_batch(float (&acc)[NV], const PT* src, float wl, int j,
                                             int m) {
   float x[U][NV];
 #pragma unroll
   for (int u = 0; u < U; ++u)
 #pragma unroll
-    for (int t = 0; t < NV; ++t) x[u][t] = u < m ? src[(j + u) * NV * 32 + 32 * t] : 0.f;
+    for (int t = 0; t < NV; ++t)
+      x[u][t] = u < m ? part_f32(src[(j + u) * NV * 32 + 32 * t]) : 0.f;
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const float w = __shfl_sync(kFull, wl, (j + u) & 31);
@@ -124,9 +130,9 @@ __device__ __forceinline__ void merge_batch(float (&acc)[NV], const float* src, 
 // Merge the nsb split partials of one output row (b, r, h) with one warp.
 // Each split s left a normalised output O_s and its log2-sum-exp L_s; the
 // result is sum_s 2^(L_s - L) O_s with L = log2 sum_s 2^(L_s).
-template <typename T, int DV>
-__device__ __forceinline__ void merge_splits(const VerifyArgs& a, int b, int r, int h, int nsb,
-                                             int lane) {
+template <typename T, int DV, typename PT>
+__device__ __forceinline__ void merge_splits(const VerifyArgs& a, const PT* parts, int b, int r,
+                                             int h, int nsb, int lane) {
   const long row = ((long)b * a.R + r) * a.Hq + h;
   const long base = (((long)b * a.Hq + h) * a.R + r) * a.nsplit;
   constexpr int NV = DV / 32;
@@ -140,7 +146,7 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, int b, int r, 
     for (int u = 0; u < kB; ++u)
 #pragma unroll
       for (int t = 0; t < NV; ++t)
-        x[u][t] = u < nsb ? a.ws_o[(base + u) * DV + lane + 32 * t] : 0.f;
+        x[u][t] = u < nsb ? part_f32(parts[(base + u) * DV + lane + 32 * t]) : 0.f;
     const float l = lane < nsb ? a.ws_lse[base + lane] : -INFINITY;
     float mx = l;
 #pragma unroll
@@ -183,7 +189,7 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, int b, int r, 
   for (int s0 = 0; s0 < nsb; s0 += 32) {
     const int n = min(32, nsb - s0);
     const float wl = lane >= n ? 0.f : exp2f((s0 == 0 ? l0 : a.ws_lse[base + s0 + lane]) - tot);
-    const float* src = a.ws_o + (base + s0) * DV + lane;
+    const PT* src = parts + (base + s0) * DV + lane;
     int j = 0;
     for (; j + kB <= n; j += kB) merge_batch<kB, NV>(acc, src, wl, j, kB);
     if (n - j > kB / 2) merge_batch<kB, NV>(acc, src, wl, j, n - j);
@@ -202,7 +208,9 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, int b, int r, 
 // workload).  It is launched with ordinary stream serialisation: launched
 // early next to a multi-wave attention grid, its CTAs slowed the following
 // kernels (5% on the batched step).
-template <typename T, int DV>
+// PT: element type of the split partials (float, or bf16 on the tcgen05 path
+// of bf16 heads).
+template <typename T, int DV, typename PT = float>
 __global__ void __launch_bounds__(128)
 verify_combine_kernel(const __grid_constant__ VerifyArgs a) {
   grid_dependency_sync();
@@ -215,7 +223,10 @@ verify_combine_kernel(const __grid_constant__ VerifyArgs a) {
   const int P = min(max(a.plen[b], 0), a.cap);
   const int nsb = P > 0 ? (P + a.split_len - 1) / a.split_len : 1;
   if (nsb == 1) return;   // a request held by one split wrote its output directly
-  merge_splits<T, DV>(a, b, r, h, nsb, lane);
+  const PT* parts;
+  if constexpr (sizeof(PT) == 2) parts = a.ws_ob;
+  else parts = a.ws_o;
+  merge_splits<T, DV, PT>(a, parts, b, r, h, nsb, lane);
 }
 
 }  // namespace

@@ -700,7 +700,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
           if (col >= rows_here) continue;
           const float res = o[e] * alpha[col];
           if (nsb == 1) ((__nv_bfloat16*)a.out)[ooff[col] + d] = __float2bfloat16_rn(res);
-          else a.ws_o[ooff[col] + d] = res;
+          else a.ws_ob[ooff[col] + d] = __float2bfloat16_rn(res);
         }
       }
     }
@@ -785,8 +785,8 @@ bool launch_tc_path(const tsd_attn_desc& d, const VerifyArgs& a, const VerifyPla
   }
   if (p.nsplit > 1) {
     const long rows = (long)a.B * a.R * a.Hq;
-    launch_plain(verify_combine_kernel<__nv_bfloat16, 128>, dim3((unsigned)ceil_div(rows, 4)),
-                 dim3(128), 0, st, a);
+    launch_plain(verify_combine_kernel<__nv_bfloat16, 128, __nv_bfloat16>,
+                 dim3((unsigned)ceil_div(rows, 4)), dim3(128), 0, st, a);
   }
   return true;
 }
