@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(kCommitThreads) commit_path_kernel(CommitArgs 
   __shared__ int s_P, s_L, s_code;
   grid_dependency_sync();
   const int b = blockIdx.x, tid = threadIdx.x;
+  // path entry tid, read together with the lengths (one memory round trip)
+  const int r_tid = tid <= a.S ? a.accept_rows[(long)b * (a.S + 1) + tid] : 0;
   // one read of the prefix and path lengths, shared by the whole CTA
   if (tid == 0) {
     s_P = a.prefix_len[b];
@@ -74,7 +76,7 @@ __global__ void __launch_bounds__(kCommitThreads) commit_path_kernel(CommitArgs 
   if (L < 0 || L > a.S) code = TSD_DEV_ERR_BAD_TREE;
   else if (P < 0 || (long)P + 1 + L > a.cap) code = TSD_DEV_ERR_CAPACITY;
   else if (tid <= L) {
-    const int r = a.accept_rows[(long)b * (a.S + 1) + tid];
+    const int r = r_tid;
     const long d0 = cache_row0(a, b, P + tid);
     if (r < 0 || r >= a.R) code = TSD_DEV_ERR_BAD_TREE;
     else if (d0 < 0) code = TSD_DEV_ERR_BAD_PAGE;

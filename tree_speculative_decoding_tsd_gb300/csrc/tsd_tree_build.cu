@@ -107,6 +107,9 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   const int R = D + 1;
   const long o = (long)b * R;
   const bool adaptive = cost_v != nullptr;
+  // the root token is loaded now, with the chunk lists, not after the merge
+  // (where the popping warp would wait for it)
+  const int32_t root = threadIdx.x == 0 ? root_tok[b] : 0;
   // adaptive mode: round cost of a tree with n nodes, fp32 C_d + C_v(n)
   if (adaptive)
     for (int n = threadIdx.x; n <= D; n += blockDim.x)
@@ -149,7 +152,7 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   }
   // row 0 = root; frontier slot 0 = rank 0 at depth 1
   if (lane == 0) {
-    s.r_sc[0] = 1.0f; s.r_par[0] = -1; s.r_tok[0] = root_tok[b]; s.r_dep[0] = 0;
+    s.r_sc[0] = 1.0f; s.r_par[0] = -1; s.r_tok[0] = root; s.r_dep[0] = 0;
     s.r_mask[0] = 0ull;
     f_sc[0] = __fmul_rn(1.0f, s.tp[0][0]); f_psc[0] = 1.0f; f_dpr[0] = pack_dpr(1, 0, 0);
     f_pm[0] = 0ull;
