@@ -326,7 +326,9 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
   fence_after();
   const uint32_t tmem = flags[0];
   if constexpr (kPaged) tiles_ready = min(n_pre, kPagedTiles);
-  const uint32_t tm_s[2] = {tmem, tmem + (uint32_t)N};
+  // S^T buffer i at column i*N (arithmetic, not an array indexed at run time,
+  // which would live in local memory)
+  auto tm_s = [&](int i) { return tmem + (uint32_t)(i * N); };
   const uint32_t tm_o = tmem + 2u * N;
 
   // ------------------------------------------------------------------ TMA
@@ -392,7 +394,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
         if (!mbar_wait(bar(BAR_K_FULL + stg), (t / kKStages) & 1, a.wait_cycles)) return false;
         fence_after();
         const uint64_t kd = kd0 + (uint64_t)(stg * (L::stage >> 4));
-        const uint32_t ts = tm_s[t & 1];
+        const uint32_t ts = tm_s(t & 1);
         mma_f16(ts, kd, qd0, idesc_qk, 0u);
 #pragma unroll
         for (int kk = 1; kk < kD / 16; ++kk)
@@ -453,7 +455,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
       fence_after();
       const bool is_tree = t >= n_pre;
       const int nvalid = is_tree ? a.R : min(kKeys, k1 - (k0 + t * kKeys));
-      const uint32_t srow = tm_s[st] + lane_off;
+      const uint32_t srow = tm_s(st) + lane_off;
       uint8_t* pt_stage = smem + L::off_k + (t % kKStages) * L::stage;
       bool pv_waited = false;                // O^T_(t-1) known complete
 
