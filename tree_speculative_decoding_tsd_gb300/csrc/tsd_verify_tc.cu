@@ -13,11 +13,15 @@
 // which delivers 128 bytes per clock to the tensor core, the TMA writes and
 // the softmax's P^T stores together: per 128-key tile that is 64 KB of K/V
 // arriving, K and Q^T read by S^T, V and P^T read by O^T, and P^T written --
-// about 236 KB at 144 packed rows, ~0.9 us at 2 GHz.  The design keeps that
-// stream busy: P^T_t is written into the ring stage that held K_t (dead once
-// S^T_t is done), so a 3-stage K ring gives P^T three buffers without more
-// shared memory, the softmax of tile t never waits for O^T_(t-1), and the
-// tensor core always has the next product queued.
+// about 236 KB at 144 packed rows, ~0.9 us at 2 GHz.  P^T_t is written into
+// the ring stage that held K_t (dead once S^T_t is done), so a 3-stage K ring
+// gives P^T three buffers without more shared memory, the softmax of tile t
+// never waits for O^T_(t-1), and the tensor core always has the next product
+// queued.  Measured (per-CTA clock stamps at every hand-off), the tile period
+// is set by the cycle of one K stage -- copy landed (~1.5 us under load),
+// S^T product, softmax (~1.3 us), O^T product, release, next copy issued --
+// divided by the three stages; the shared-memory capacity (Q^T, three K/P^T
+// stages, two V stages) leaves no room for a fourth.
 //
 // Roles (608 threads): warps 0-15 softmax/epilogue (warpgroup w/4 owns a
 // quarter of the columns, warp w%4 owns TMEM lanes 32(w%4)..+31, i.e. 32 keys
