@@ -72,9 +72,10 @@ __device__ __forceinline__ bool precedes(float sa, int da, uint64_t a0, uint64_t
 }
 
 // Per-lane register slots: frontier entry e lives in lane e % 32, slot e / 32.
-// The frontier never holds more than D + 1 entries, so ceil((D + 2) / 32)
-// slots suffice; the kernel is instantiated for 1, 2 and 3 slots (D <= 30,
-// 62, 64) because every pick and put costs one select per slot.
+// A pop removes one entry and adds at most two (net +1), and the last pop
+// adds none, so pop r reads at most r entries and writes index <= r - 1 < D:
+// ceil(D / 32) slots suffice; the kernel is instantiated for 1 and 2 slots
+// (D <= 32, D <= 64) because every pick and put costs one select per slot.
 template <int NS, typename T>
 __device__ __forceinline__ T pick(const T (&v)[NS], int j) {
   T r = v[0];
@@ -231,6 +232,9 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       s.r_dep[row] = d;
       s.r_mask[row] = m;
     }
+    // nothing is popped after the last row: no new entries (so the frontier
+    // never holds more than D entries when a pop reads it)
+    if (row == D) break;
     // the popped slot becomes the next sibling, or takes the last entry
     const int bl = best & 31, bj = best >> 5;
     const int last = nf - 1;
@@ -332,9 +336,7 @@ tsd_status tree_build_impl(const float* probs, int B, int S, int V, int k, int D
   uint64_t* part = (uint64_t*)ws;
   launch(vocab_scan_kernel<false>, dim3((unsigned)ctas), dim3(kScanThreads), 0, st, probs, V, k,
       g.nchunk, g.chunk_len, part, g.one_wave, err, S);
-  const auto tree_kernel = D + 2 <= 32   ? best_first_tree_kernel<1>
-                           : D + 2 <= 64 ? best_first_tree_kernel<2>
-                                         : best_first_tree_kernel<3>;
+  const auto tree_kernel = D <= 32 ? best_first_tree_kernel<1> : best_first_tree_kernel<2>;
   launch(tree_kernel, dim3(B), dim3(32 * S), 0, st, part, S, k, D, g.nchunk, root_tok, token,
       parent, depth, score, mask, is_leaf, cost_d, cost_v, n_nodes);
   return cuda_status();
