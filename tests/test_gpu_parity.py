@@ -113,6 +113,10 @@ def test_tree_build_full_size(name):
     (2, 3, 32, 32, 40, 16),         # V == k: every token kept, ties
     (3, 2, 200000, 4, 9, None),     # long rows over many chunks
     (2, 3, 50000, 8, 20, 1),        # every probability rounds to 0: all elements tie
+    # register slots of the frontier: ceil(D / 32), the frontier growing by one
+    # entry per pop (a sibling and a child each time) up to D entries
+    (2, 16, 600, 32, 31, None), (2, 16, 600, 32, 32, None), (2, 16, 600, 32, 33, None),
+    (2, 16, 600, 32, 63, None), (2, 16, 600, 32, 64, None), (2, 16, 600, 32, 64, 64),
 ])
 def test_tree_build_edge_cases(B, S, V, k, D, quant):
     g = torch.Generator().manual_seed(B * 1000 + S * 100 + k)
