@@ -98,13 +98,14 @@ __device__ __forceinline__ void warp_list_offer(uint64_t& entry, uint64_t& thr, 
   }
 }
 
+// Warp maximum of 64-bit keys: two 32-bit hardware reductions (the high word,
+// then the low word among the lanes holding the highest high word) instead
+// of five rounds of 64-bit shuffles.
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t w = __shfl_xor_sync(kFull, v, o);
-    v = w > v ? w : v;
-  }
-  return v;
+  const uint32_t hi = (uint32_t)(v >> 32), lo = (uint32_t)v;
+  const uint32_t hmax = __reduce_max_sync(kFull, hi);
+  const uint32_t lmax = __reduce_max_sync(kFull, hi == hmax ? lo : 0u);
+  return ((uint64_t)hmax << 32) | lmax;
 }
 
 // Top-k of the 32*NC candidates held by the warp (NC per lane), returned as
