@@ -7,14 +7,18 @@
 // the row's top-k is the top-k of the union of its chunks' top-k lists, which
 // is exact because candidates are distinct.
 //
-// Top-k mode reads the chunk once from HBM, keeping only a running maximum
-// per thread.  The k-th largest of the 256 thread maxima, T, is a cut-off:
-// k distinct elements are >= T, so every element of the chunk's top-k is
-// >= T, and only threads whose maximum reaches T hold any such element
-// (about k of the 256).  The warp re-reads just those threads' elements (from
-// L2, where the first pass left them) and offers the ones >= T to a sorted
-// warp list; the CTA then merges its eight warp lists.  NaN entries are never
-// selected.
+// Top-k mode reads the chunk once from HBM; each thread keeps its best
+// element (value and index) and its second largest value.  The k best of the
+// 256 thread candidates are the chunk's top-k whenever no thread's second
+// value reaches the k-th of them (every other element is then below its
+// thread's best and below the k-th candidate) -- the common case, which needs
+// no second look at the data.  Otherwise (two top-k elements in one thread,
+// ties, or fewer than k elements) the k-th candidate's value T is a cut-off:
+// k distinct elements are >= T, so the top-k is >= T and only threads whose
+// best reaches T hold any of it; the warp re-reads just those threads'
+// elements (from L2, where the first pass left them) and offers the ones >= T
+// to a sorted warp list, and the CTA merges its eight warp lists.  NaN
+// entries are never selected.
 // Top-k mode also checks that the row is a probability vector as the tree
 // rule needs it (no value above 1, no NaN) and reports a violation in the
 // caller's error word.
@@ -84,8 +88,8 @@ __global__ void __launch_bounds__(kScanThreads, kArgmax ? kScanArgmaxPerSm : kSc
 vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chunk_len,
                   uint64_t* __restrict__ out, int prefetch, int32_t* err, int rows_per_req) {
   __shared__ uint64_t s_list[kScanWarps][32];
-  __shared__ float s_max[kScanThreads];
-  __shared__ float s_cut;
+  __shared__ uint64_t s_key[kScanThreads];
+  __shared__ uint64_t s_wk;
 
   const long cta = blockIdx.x;
   const long row = cta / nchunk;
@@ -157,11 +161,26 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
   }
 
   // ---- top-k mode -------------------------------------------------------
-  // pass 1: stream the vector part once, one running maximum per thread
-  // (NaN ignored), and one that keeps NaN (for the range check)
-  // (eight 16-byte loads in flight per thread: with about three CTAs per SM
-  // that is what keeps enough bytes in flight to stream at HBM speed)
-  float m = -INFINITY, mn = -INFINITY;
+  // pass 1: stream the chunk once.  Each thread keeps its best element (the
+  // largest value, its first index on ties: the candidate order), the second
+  // largest value among its elements, and a maximum that keeps NaN (for the
+  // range check); NaN is never taken.  (Eight 16-byte loads in flight per
+  // thread: with about three CTAs per SM that keeps enough bytes in flight to
+  // stream at HBM speed.)  A thread's elements are visited in increasing
+  // index order: its front edge element, its float4s, its back edge element.
+  float m = -INFINITY, m2 = -INFINITY, mn = -INFINITY;
+  int mi = -1;
+  auto take = [&](float x, int i) {
+    const bool gt = x > m;
+    m2 = gt ? m : fmaxf(m2, x);
+    mi = gt ? i : mi;
+    m = gt ? x : m;
+  };
+  if (c0 + tid < a0) {
+    const float x = xr[c0 + tid];
+    take(x, c0 + tid);
+    mn = max3_nan(mn, x, -INFINITY);
+  }
   {
     constexpr int U = 8;
     int v = tid;
@@ -171,7 +190,8 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
       for (int u = 0; u < U; ++u) f[u] = __ldg(xv + v + u * kScanThreads);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        m = fmaxf(m, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
+        const int i0 = a0 + 4 * (v + u * kScanThreads);
+        take(f[u].x, i0); take(f[u].y, i0 + 1); take(f[u].z, i0 + 2); take(f[u].w, i0 + 3);
         mn = max3_nan(mn, max3_nan(f[u].x, f[u].y, f[u].z), f[u].w);
       }
     }
@@ -182,16 +202,47 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
                                          : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 #pragma unroll
     for (int u = 0; u < U - 1; ++u) {
-      m = fmaxf(m, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
+      const int i0 = a0 + 4 * (v + u * kScanThreads);
+      take(f[u].x, i0); take(f[u].y, i0 + 1); take(f[u].z, i0 + 2); take(f[u].w, i0 + 3);
       mn = max3_nan(mn, max3_nan(f[u].x, f[u].y, f[u].z), f[u].w);
     }
   }
-  s_max[tid] = m;
-  for (int i = c0 + tid; i < a0; i += kScanThreads) mn = max3_nan(mn, xr[i], -INFINITY);
-  for (int i = a1 + tid; i < c1; i += kScanThreads) mn = max3_nan(mn, xr[i], -INFINITY);
+  if (a1 + tid < c1) {
+    const float x = xr[a1 + tid];
+    take(x, a1 + tid);
+    mn = max3_nan(mn, x, -INFINITY);
+  }
   // a value above 1 (or NaN) breaks the score order the tree build relies on
   if (err != nullptr && __any_sync(kFull, !(mn <= 1.0f)) && lane == 0)
     report_error(err, TSD_DEV_ERR_BAD_PROBS, (int)(row / rows_per_req));
+
+  // The k best of the 256 thread candidates, in order (warp 0, k rounds of a
+  // warp maximum).  They are the chunk's top-k unless a thread holds a second
+  // element that could rank among them (its second largest value reaches the
+  // k-th candidate's value) or fewer than k threads hold an element: every
+  // other element is below its thread's best and below the k-th candidate.
+  s_key[tid] = mi >= 0 ? make_cand(m, (uint32_t)mi) : 0ull;
+  __syncthreads();
+  if (warp == 0) {
+    uint64_t c[kScanThreads / 32];
+#pragma unroll
+    for (int j = 0; j < kScanThreads / 32; ++j) c[j] = s_key[j * 32 + lane];
+    const uint64_t best = warp_topk<kScanThreads / 32>(c, k, lane);
+    const uint64_t wk = __shfl_sync(kFull, best, k - 1);
+    if (lane < k) s_key[lane] = best;           // (all reads of s_key above are done)
+    if (lane == 0) s_wk = wk;
+  }
+  __syncthreads();
+  const uint64_t wk = s_wk;
+  const bool more = wk == 0ull || m2 >= cand_val(wk);
+  if (!__syncthreads_or(more)) {
+    if (warp == 0 && lane < k) out[cta * k + lane] = s_key[lane];
+    return;
+  }
+
+  // Otherwise the rescans: cut-off T = the k-th candidate's value (k
+  // distinct elements are >= T, so the chunk's top-k is >= T).
+  const float cut = wk == 0ull ? -INFINITY : cand_val(wk);
 
   // the (at most 3 + 3) scalar edge elements are offered to the warp list directly
   const unsigned kmask = (k >= 32) ? kFull : ((1u << k) - 1u);
@@ -208,39 +259,9 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
     const uint64_t c = (i < c1 && x == x) ? make_cand(x, i) : 0ull;
     warp_list_offer(entry, thr, c, k, kmask, lane);
   }
-  __syncthreads();
-
-  // cut-off T: the k-th largest of the 256 thread maxima (k <= 32 < 256), by
-  // k rounds of a warp maximum over 32-bit order keys; each round removes one
-  // occurrence of the winner
-  if (warp == 0) {
-    uint32_t c[kScanThreads / 32];
-#pragma unroll
-    for (int j = 0; j < kScanThreads / 32; ++j) c[j] = f32_order_key(s_max[j * 32 + lane]);
-    uint32_t w = 0;
-    for (int r = 0; r < k; ++r) {
-      uint32_t lm = c[0];
-#pragma unroll
-      for (int j = 1; j < kScanThreads / 32; ++j) lm = max(lm, c[j]);
-      w = __reduce_max_sync(kFull, lm);
-      const unsigned who = __ballot_sync(kFull, lm == w);
-      if (lane == __ffs(who) - 1) {
-        bool done = false;
-#pragma unroll
-        for (int j = 0; j < kScanThreads / 32; ++j) {
-          const bool hit = !done && c[j] == w;
-          c[j] = hit ? 0u : c[j];
-          done = done || hit;
-        }
-      }
-    }
-    if (lane == 0) s_cut = order_key_f32(w);
-  }
-  __syncthreads();
 
   // pass 2: the warp re-reads, one thread at a time, the elements of its
   // threads whose maximum reaches T: lane j takes that thread's j-th float4
-  const float cut = s_cut;
   unsigned act = __ballot_sync(kFull, m >= cut);
   while (act) {
     const int t = warp * 32 + __ffs(act) - 1;
