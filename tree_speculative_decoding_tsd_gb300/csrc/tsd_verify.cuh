@@ -96,6 +96,72 @@ template <> __device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(floa
   return __float2bfloat16_rn(x);
 }
 
+// NV consecutive elements (NV = 2, 4, 8 or 16) at p, 4 * NV-byte or
+// 2 * NV-byte aligned: vector loads and stores.
+template <int NV>
+__device__ __forceinline__ void load_vec(const float* p, float (&x)[NV]) {
+  if constexpr (NV == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    x[0] = v.x; x[1] = v.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < NV; i += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(p + i);
+      x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
+    }
+  }
+}
+template <int NV>
+__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float (&x)[NV]) {
+  constexpr int W = NV >= 8 ? 8 : NV;                 // bf16 per load
+#pragma unroll
+  for (int i = 0; i < NV; i += W) {
+    uint32_t w[W / 2];
+    if constexpr (W == 8) {
+      const uint4 v = *reinterpret_cast<const uint4*>(p + i);
+      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (W == 4) {
+      const uint2 v = *reinterpret_cast<const uint2*>(p + i);
+      w[0] = v.x; w[1] = v.y;
+    } else {
+      w[0] = *reinterpret_cast<const uint32_t*>(p + i);
+    }
+#pragma unroll
+    for (int j = 0; j < W / 2; ++j) {
+      x[i + 2 * j] = __uint_as_float(w[j] << 16);
+      x[i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  }
+}
+template <int NV>
+__device__ __forceinline__ void store_vec(float* p, const float (&x)[NV]) {
+  if constexpr (NV == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NV; i += 4)
+      *reinterpret_cast<float4*>(p + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+  }
+}
+template <int NV>
+__device__ __forceinline__ void store_vec(__nv_bfloat16* p, const float (&x)[NV]) {
+  uint32_t w[NV / 2];
+#pragma unroll
+  for (int j = 0; j < NV / 2; ++j) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
+    w[j] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  if constexpr (NV == 2) {
+    *reinterpret_cast<uint32_t*>(p) = w[0];
+  } else if constexpr (NV == 4) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NV / 2; i += 4)
+      *reinterpret_cast<uint4*>(p + 2 * i) = make_uint4(w[i], w[i + 1], w[i + 2], w[i + 3]);
+  }
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
@@ -139,14 +205,19 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, const PT* part
   constexpr int kB = NV > 4 ? 4 : 8;
   // A row of at most kB splits (the common case) has its partials' loads
   // issued together with the log-sum-exp loads, before the weights are known:
-  // one memory round trip instead of two.
+  // one memory round trip instead of two.  Lane j takes the NV consecutive
+  // dims NV*j .. NV*j+NV-1 (vector loads and stores).
   if (nsb <= kB) {
     float x[kB][NV];
 #pragma unroll
-    for (int u = 0; u < kB; ++u)
+    for (int u = 0; u < kB; ++u) {
+      if (u < nsb) {
+        load_vec<NV>(parts + (base + u) * DV + NV * lane, x[u]);
+      } else {
 #pragma unroll
-      for (int t = 0; t < NV; ++t)
-        x[u][t] = u < nsb ? part_f32(parts[(base + u) * DV + lane + 32 * t]) : 0.f;
+        for (int t = 0; t < NV; ++t) x[u][t] = 0.f;
+      }
+    }
     const float l = lane < nsb ? a.ws_lse[base + lane] : -INFINITY;
     float mx = l;
 #pragma unroll
@@ -164,8 +235,7 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, const PT* part
         for (int t = 0; t < NV; ++t) acc[t] = fmaf(w, x[u][t], acc[t]);
       }
     }
-#pragma unroll
-    for (int t = 0; t < NV; ++t) ((T*)a.out)[row * DV + lane + 32 * t] = cvt_out<T>(acc[t]);
+    store_vec<NV>((T*)a.out + row * DV + NV * lane, acc);
     if (lane == 0) a.lse[row] = tot * 0.69314718055994531f;
     return;
   }
