@@ -268,6 +268,12 @@ VerifyPlan plan_verify(const tsd_attn_desc& d) {
     p.split_len = (int)ceil_div(d.cap, ns);
   }
   p.nsplit = (int)ceil_div(d.cap, p.split_len);
+  // Short splits of the tcgen05 path of bf16 heads: the tree tile gets a split
+  // (a CTA) of its own instead of lengthening the last prefix split, which is
+  // the critical path when a split is a few tiles (qwen-sized step: 2 prefix
+  // tiles per split).
+  p.tree_split = (p.path == kPathTc && !d.v_aliases_k && p.nsplit > 1 && p.split_len <= 1024) ? 1 : 0;
+  if (p.tree_split) ++p.nsplit;
   // The tcgen05 path of bf16 heads stores its split partials in bf16 (the
   // normalised partial output of a split is a convex combination of bf16
   // values; the merge weights stay fp32), halving the partials' traffic.
@@ -380,6 +386,7 @@ static tsd_status verify_impl(const tsd_attn_desc* d, const void* q, const void*
   a.B = d->B; a.R = d->R; a.Hq = d->Hq; a.Hkv = d->Hkv; a.g = d->Hq / d->Hkv;
   a.M = d->R * a.g; a.cap = d->cap;
   a.nsplit = p.nsplit; a.split_len = p.split_len; a.nrg = p.nrg;
+  a.tree_split = p.tree_split;
   a.qscale = d->scale * 1.4426950408889634f;
   a.err = err;
   {

@@ -30,6 +30,7 @@ struct VerifyArgs {
   long long wait_cycles;   // budget of the tcgen05 kernels' pipeline waits (clock cycles)
   int B, R, Hq, Hkv, g, M, cap;
   int nsplit, split_len, nrg;
+  int tree_split;  // 1: the tree tile is a split of its own (after the prefix splits)
   float qscale;   // softmax scale * log2(e): scores are kept in the log2 domain
   // paged cache (page_size > 0): kc/vc are page pools [num_pages][Hkv][page_size][d]
   // and key `pos` of request b lives in page page_table[b][pos / page_size]
@@ -46,6 +47,7 @@ struct VerifyPlan {
   int nsplit;     // prefix splits (grid x); a request uses ceil(P / split_len)
   int split_len;
   int part_bf16;  // split partials stored in bf16 (1) or fp32 (0)
+  int tree_split;  // the tree tile is a split of its own
   size_t ws_bytes;
 };
 
@@ -160,6 +162,13 @@ __device__ __forceinline__ void store_vec(__nv_bfloat16* p, const float (&x)[NV]
     for (int i = 0; i < NV / 2; i += 4)
       *reinterpret_cast<uint4*>(p + 2 * i) = make_uint4(w[i], w[i + 1], w[i + 2], w[i + 3]);
   }
+}
+
+// Splits that hold work for a request with prefix P: the prefix splits, and
+// the tree tile either in the last of them or (tree_split) after them.
+__device__ __forceinline__ int verify_splits(const VerifyArgs& a, int P) {
+  const int npre = P > 0 ? (P + a.split_len - 1) / a.split_len : 0;
+  return a.tree_split ? npre + 1 : max(npre, 1);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -291,7 +300,7 @@ verify_combine_kernel(const __grid_constant__ VerifyArgs a) {
   const int r = (int)((row / a.Hq) % a.R);
   const int h = (int)(row % a.Hq);
   const int P = min(max(a.plen[b], 0), a.cap);
-  const int nsb = P > 0 ? (P + a.split_len - 1) / a.split_len : 1;
+  const int nsb = verify_splits(a, P);
   if (nsb == 1) return;   // a request held by one split wrote its output directly
   const PT* parts;
   if constexpr (sizeof(PT) == 2) parts = a.ws_ob;

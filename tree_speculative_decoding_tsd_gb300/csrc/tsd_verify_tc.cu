@@ -224,9 +224,10 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
     b = (int)flags[2];
   }
   const int P = min(max(a.plen[b], 0), a.cap);
-  const int nsb = P > 0 ? (P + a.split_len - 1) / a.split_len : 1;
+  const int nsb = verify_splits(a, P);
   if (sp >= nsb) return;  // uniform for the whole CTA, before any barrier or allocation
-  const int k0 = sp * a.split_len, k1 = min(P, k0 + a.split_len);
+  // (a tree-only split starts at P: no prefix tiles)
+  const int k0 = min(sp * a.split_len, P), k1 = min(P, k0 + a.split_len);
   const int n_pre = k1 > k0 ? (k1 - k0 + kKeys - 1) / kKeys : 0;
   const int n_tree = (sp == nsb - 1) ? 1 : 0;   // R <= 65 < 128: one tile
   const int ntiles = n_pre + n_tree;
