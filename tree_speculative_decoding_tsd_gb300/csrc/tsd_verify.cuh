@@ -211,15 +211,16 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, const PT* part
   const long row = ((long)b * a.R + r) * a.Hq + h;
   const long base = (((long)b * a.Hq + h) * a.R + r) * a.nsplit;
   constexpr int NV = DV / 32;
-  constexpr int kB = NV > 4 ? 4 : 8;
-  // A row of at most kB splits (the common case) has its partials' loads
+  constexpr int kB = NV > 4 ? 4 : 8;          // partials per batch of loads
+  constexpr int kF = NV > 4 ? 4 : 16;         // splits of the one-round-trip path
+  // A row of at most kF splits (the common case) has its partials' loads
   // issued together with the log-sum-exp loads, before the weights are known:
   // one memory round trip instead of two.  Lane j takes the NV consecutive
   // dims NV*j .. NV*j+NV-1 (vector loads and stores).
-  if (nsb <= kB) {
-    float x[kB][NV];
+  if (nsb <= kF) {
+    float x[kF][NV];
 #pragma unroll
-    for (int u = 0; u < kB; ++u) {
+    for (int u = 0; u < kF; ++u) {
       if (u < nsb) {
         load_vec<NV>(parts + (base + u) * DV + NV * lane, x[u]);
       } else {
@@ -237,7 +238,7 @@ __device__ __forceinline__ void merge_splits(const VerifyArgs& a, const PT* part
 #pragma unroll
     for (int t = 0; t < NV; ++t) acc[t] = 0.f;
 #pragma unroll
-    for (int u = 0; u < kB; ++u) {
+    for (int u = 0; u < kF; ++u) {
       const float w = __shfl_sync(kFull, wl, u);
       if (u < nsb) {
 #pragma unroll
