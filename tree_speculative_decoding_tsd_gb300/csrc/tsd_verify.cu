@@ -219,6 +219,11 @@ VerifyPlan plan_verify(const tsd_attn_desc& d) {
   } else if (p.path == kPathTc) {
     // packed rows on the MMA N dimension: at most 144 per CTA, multiple of 16
     p.nrg = (int)ceil_div(M, 144);
+    // A grid that fills at most half the GPU with 256-key splits (a small
+    // batch) takes twice the row groups: CTAs of fewer columns, a shorter
+    // critical path (qwen-sized step 39.8 -> 38.8 us; the second CTA of a
+    // tile finds it in L2).
+    if ((long)d.B * d.Hkv * p.nrg * ceil_div(d.cap, 256) <= 76 && M >= 32) p.nrg *= 2;
     p.rb = (int)ceil_div(ceil_div(M, p.nrg), 16) * 16;
     // Splits.  A small batch takes about two waves of CTAs: splits of 256 to
     // 4096 keys, the shorter ones shortening the critical path (qwen-sized
