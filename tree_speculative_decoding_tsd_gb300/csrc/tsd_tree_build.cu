@@ -37,8 +37,10 @@ struct TreeSmem {
   float tp[kMaxS][kMaxK];     // top-k probabilities per position
   int32_t ti[kMaxS][kMaxK];   // top-k token ids per position
   float cost[kMaxD + 1];      // adaptive mode: C_d + C_v(n), n = 0..D
-  // the tree's rows, written by lane 0 as they are popped
+  // the tree's rows, written as they are popped (by every lane of the
+  // popping warp, so that each lane reads back only its own writes)
   uint64_t r_mask[kMaxD + 1];
+  uint64_t r_w0[kMaxD + 1], r_w1[kMaxD + 1];   // rank tuples
   float r_sc[kMaxD + 1];
   int32_t r_par[kMaxD + 1];
   int32_t r_tok[kMaxD + 1];
@@ -53,12 +55,6 @@ __device__ __forceinline__ void tuple_add(uint64_t& w0, uint64_t& w1, int level,
   else w1 += digit << (59 - 5 * (level - 12));
 }
 
-// Primary key of a frontier entry: the score's bit pattern inverted (the bit
-// pattern of a non-negative float grows with it), so the smallest key is the
-// highest score.  Entries with different keys are ordered by the key alone;
-// equal keys (equal scores) are resolved by the full comparison.
-__device__ __forceinline__ uint32_t score_key(float sc) { return ~__float_as_uint(sc); }
-
 // Depth, parent row and rank of a frontier entry in one word (each < 256).
 __device__ __forceinline__ int pack_dpr(int d, int par, int rk) { return d | (par << 8) | (rk << 16); }
 
@@ -71,28 +67,11 @@ __device__ __forceinline__ bool precedes(float sa, int da, uint64_t a0, uint64_t
   return a1 < b1;
 }
 
-// Per-lane register slots: frontier entry e lives in lane e % 32, slot e / 32.
-// A pop removes one entry and adds at most two (net +1), and the last pop
-// adds none, so pop r reads at most r entries and writes index <= r - 1 < D:
-// ceil(D / 32) slots suffice; the kernel is instantiated for 1 and 2 slots
-// (D <= 32, D <= 64) because every pick and put costs one select per slot.
-template <int NS, typename T>
-__device__ __forceinline__ T pick(const T (&v)[NS], int j) {
-  T r = v[0];
-#pragma unroll
-  for (int i = 1; i < NS; ++i) r = (j == i) ? v[i] : r;
-  return r;
-}
-template <int NS, typename T>
-__device__ __forceinline__ void put(T (&v)[NS], int j, T x, bool pred) {
-#pragma unroll
-  for (int i = 0; i < NS; ++i) v[i] = (pred && j == i) ? x : v[i];
-}
-template <int NS, typename T>
-__device__ __forceinline__ T bcast(const T (&v)[NS], int e) {
-  return __shfl_sync(kFull, pick<NS>(v, e >> 5), e & 31);
-}
-
+// The frontier minus its best entry is a sorted list spread over the lanes,
+// entry e in lane e % 32, slot e / 32.  A pop removes one entry and adds at
+// most two (net +1), and the last pop adds none, so before pop r the frontier
+// holds at most r entries and the list at most D - 1: ceil(D / 32) slots
+// suffice (1 for D <= 32, 2 for D <= 64).
 template <int kSlots>
 __global__ void __launch_bounds__(32 * kMaxS, 1)
 best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, int nchunk,
@@ -138,138 +117,133 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   __syncthreads();
   if (warp != 0) return;
 
-  // ---- frontier in registers, spread over the lanes; rows in shared memory ----
-  // A frontier entry also carries its parent's score and ancestor mask, so a
-  // pop needs no lookup of the parent row.  Lane 0 writes each popped row to
-  // shared memory (no per-lane selects on the critical path).
-  float f_sc[kSlots], f_psc[kSlots];
-  uint32_t f_key[kSlots];
-  int32_t f_dpr[kSlots];
-  uint64_t f_w0[kSlots], f_w1[kSlots], f_pm[kSlots];
+  // ---- the pops: one warp, rows in shared memory ----
+  // An entry is (score, depth | parent row << 8 | rank << 16).  Its rank
+  // tuple is its parent row's tuple with its rank added at its depth, so the
+  // tuple is looked up (rows keep theirs) only where scores tie.  The best
+  // entry not yet popped (t_*) is held by every lane; the rest of the
+  // frontier is the sorted list L (l_*).  A pop's sibling and child go to
+  // the places given by the count of L's entries before them (ballots: L is
+  // sorted), and the new best entry and the new L are read off the merged
+  // list, each lane gathering its new entry with one shuffle per slot.
+  float l_sc[kSlots];
+  int32_t l_dpr[kSlots];
 #pragma unroll
-  for (int j = 0; j < kSlots; ++j) {
-    f_sc[j] = 0.f; f_psc[j] = 0.f; f_key[j] = ~0u; f_dpr[j] = 0;
-    f_w0[j] = 0ull; f_w1[j] = 0ull; f_pm[j] = 0ull;
-  }
-  // row 0 = root; frontier slot 0 = rank 0 at depth 1
-  if (lane == 0) {
-    s.r_sc[0] = 1.0f; s.r_par[0] = -1; s.r_tok[0] = root; s.r_dep[0] = 0;
-    s.r_mask[0] = 0ull;
-    f_sc[0] = __fmul_rn(1.0f, s.tp[0][0]); f_psc[0] = 1.0f; f_dpr[0] = pack_dpr(1, 0, 0);
-    f_pm[0] = 0ull;
-    f_key[0] = score_key(f_sc[0]);
-  }
-  int nf = 1;
+  for (int j = 0; j < kSlots; ++j) { l_sc[j] = 0.f; l_dpr[j] = pack_dpr(1, 0, 0); }
+  // row 0 = root
+  s.r_sc[0] = 1.0f; s.r_par[0] = -1; s.r_tok[0] = __shfl_sync(kFull, root, 0);
+  s.r_dep[0] = 0; s.r_mask[0] = 0ull; s.r_w0[0] = 0ull; s.r_w1[0] = 0ull;
+  // the first entry: rank 0 at depth 1
+  float t_sc = __fmul_rn(1.0f, s.tp[0][0]);
+  int32_t t_dpr = pack_dpr(1, 0, 0);
+  int nl = 0;
   // Phi accumulation for the adaptive stop: A = 1 + Phi(first n nodes), fp32
   // in pop order.  Node n+1 is kept iff (A + s) * cost[n] > A * cost[n+1]
   // (fp32 products, i.e. the objective rises); the first failure ends the tree.
   float acc = 1.0f;
   int kept = D;
+  constexpr int kNone = 1 << 20;   // place of a candidate that is not inserted
 
   for (int row = 1; row <= D; ++row) {
-    // this lane's smallest key, then the warp's; one holder of one entry is
-    // the common case, several entries with the key (equal scores) take the
-    // full comparison
-    uint32_t kmin = ~0u;
-    int mine = -1;
-#pragma unroll
-    for (int j = 0; j < kSlots; ++j) {
-      const int e = lane + 32 * j;
-      // (a score of 0 has the key ~0u, so "no entry yet" is mine < 0)
-      if (e < nf && (mine < 0 || f_key[j] < kmin)) { kmin = f_key[j]; mine = e; }
-    }
-    const uint32_t hmin = __reduce_min_sync(kFull, kmin);
-    int ties = 0;
-#pragma unroll
-    for (int j = 0; j < kSlots; ++j) ties += (lane + 32 * j < nf && f_key[j] == hmin) ? 1 : 0;
-    const unsigned hb = __ballot_sync(kFull, ties > 0);
-    const unsigned hm = __ballot_sync(kFull, ties > 1);
-    int best = __shfl_sync(kFull, mine, __ffs(hb) - 1);
-    if (__popc(hb) > 1 || hm != 0u) {
-      // equal scores: full order (depth, then rank tuple)
-      int b2 = -1;
-      float bs = 0.f; int bd = 0; uint64_t b0 = 0ull, b1 = 0ull;
-#pragma unroll
-      for (int j = 0; j < kSlots; ++j) {
-        const int e = lane + 32 * j;
-        const int dj = f_dpr[j] & 0xff;
-        if (e < nf && f_key[j] == hmin &&
-            (b2 < 0 || precedes(f_sc[j], dj, f_w0[j], f_w1[j], bs, bd, b0, b1))) {
-          b2 = e; bs = f_sc[j]; bd = dj; b0 = f_w0[j]; b1 = f_w1[j];
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const int oe = __shfl_xor_sync(kFull, b2, off);
-        const float os = __shfl_xor_sync(kFull, bs, off);
-        const int od = __shfl_xor_sync(kFull, bd, off);
-        const uint64_t o0 = __shfl_xor_sync(kFull, b0, off), o1 = __shfl_xor_sync(kFull, b1, off);
-        if (oe >= 0 && (b2 < 0 || precedes(os, od, o0, o1, bs, bd, b0, b1))) {
-          b2 = oe; bs = os; bd = od; b0 = o0; b1 = o1;
-        }
-      }
-      best = b2;
-    }
-    // the popped entry and the new row
-    const float sc = bcast<kSlots>(f_sc, best), psc = bcast<kSlots>(f_psc, best);
+    const int d = t_dpr & 0xff, par = (t_dpr >> 8) & 0xff, rk = t_dpr >> 16;
+    const bool sib = rk + 1 < k, child = d < S;
+    // this pop's reads, issued together
+    const float psc = s.r_sc[par];
+    const float q_sib = s.tp[d - 1][sib ? rk + 1 : rk];
+    const float q_child = s.tp[child ? d : d - 1][0];
+    const uint64_t pm = s.r_mask[par];
+    uint64_t t_w0 = s.r_w0[par], t_w1 = s.r_w1[par];
+    const int32_t tok = s.ti[d - 1][rk];
+    const float h_sc = __shfl_sync(kFull, l_sc[0], 0);     // L[0]
+    const int32_t h_dpr = __shfl_sync(kFull, l_dpr[0], 0);
     if (adaptive) {
-      const float acc1 = __fadd_rn(acc, sc);
+      const float acc1 = __fadd_rn(acc, t_sc);
       if (!(__fmul_rn(acc1, s.cost[row - 1]) > __fmul_rn(acc, s.cost[row]))) {
         kept = row - 1;
         break;
       }
       acc = acc1;
     }
-    const int dpr = bcast<kSlots>(f_dpr, best);
-    const int d = dpr & 0xff, par = (dpr >> 8) & 0xff, rk = dpr >> 16;
-    const uint64_t w0 = bcast<kSlots>(f_w0, best), w1 = bcast<kSlots>(f_w1, best);
-    const uint64_t pm = bcast<kSlots>(f_pm, best);
-    const uint64_t m = pm | (1ull << (row - 1));
-    if (lane == 0) {
-      s.r_sc[row] = sc;
-      s.r_par[row] = par;
-      s.r_tok[row] = s.ti[d - 1][rk];
-      s.r_dep[row] = d;
-      s.r_mask[row] = m;
-    }
-    // nothing is popped after the last row: no new entries (so the frontier
-    // never holds more than D entries when a pop reads it)
+    tuple_add(t_w0, t_w1, d - 1, (uint64_t)rk);
+    s.r_sc[row] = t_sc;
+    s.r_par[row] = par;
+    s.r_tok[row] = tok;
+    s.r_dep[row] = d;
+    s.r_mask[row] = pm | (1ull << (row - 1));
+    s.r_w0[row] = t_w0;
+    s.r_w1[row] = t_w1;
+    // nothing is popped after the last row: no new entries
     if (row == D) break;
-    // the popped slot becomes the next sibling, or takes the last entry
-    const int bl = best & 31, bj = best >> 5;
-    const int last = nf - 1;
-    if (rk + 1 < k) {
-      const float nsc = __fmul_rn(psc, s.tp[d - 1][rk + 1]);
-      uint64_t nw0 = w0, nw1 = w1;
-      tuple_add(nw0, nw1, d - 1, 1ull);
-      const bool me = lane == bl;
-      put<kSlots>(f_sc, bj, nsc, me); put<kSlots>(f_dpr, bj, pack_dpr(d, par, rk + 1), me);
-      put<kSlots>(f_w0, bj, nw0, me); put<kSlots>(f_w1, bj, nw1, me);
-      put<kSlots>(f_key, bj, score_key(nsc), me);
-    } else {
-      const float lsc = bcast<kSlots>(f_sc, last), lps = bcast<kSlots>(f_psc, last);
-      const int ldpr = bcast<kSlots>(f_dpr, last);
-      const uint64_t l0 = bcast<kSlots>(f_w0, last), l1 = bcast<kSlots>(f_w1, last);
-      const uint32_t lk = bcast<kSlots>(f_key, last);
-      const uint64_t lm = bcast<kSlots>(f_pm, last);
-      const bool me = lane == bl;
-      put<kSlots>(f_sc, bj, lsc, me); put<kSlots>(f_psc, bj, lps, me);
-      put<kSlots>(f_dpr, bj, ldpr, me); put<kSlots>(f_w0, bj, l0, me);
-      put<kSlots>(f_w1, bj, l1, me); put<kSlots>(f_key, bj, lk, me); put<kSlots>(f_pm, bj, lm, me);
-      nf = last;
+
+    // the candidates: next sibling (depth d, rank rk + 1), first child
+    // (depth d + 1, rank 0); on equal scores the sibling, less deep, first
+    const float c1 = __fmul_rn(psc, q_sib), c2 = __fmul_rn(t_sc, q_child);
+    const int32_t c1_dpr = pack_dpr(d, par, rk + 1), c2_dpr = pack_dpr(d + 1, row, 0);
+    // their places in L: the entries of higher score, then of equal score
+    // (those take the full order)
+    int gt1 = 0, ge1 = 0, gt2 = 0, ge2 = 0;
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j) {
+      const bool v = lane + 32 * j < nl;
+      gt1 += __popc(__ballot_sync(kFull, v && l_sc[j] > c1));
+      ge1 += __popc(__ballot_sync(kFull, v && l_sc[j] >= c1));
+      gt2 += __popc(__ballot_sync(kFull, v && l_sc[j] > c2));
+      ge2 += __popc(__ballot_sync(kFull, v && l_sc[j] >= c2));
     }
-    // first child (rank 0 at the next position)
-    if (d < S) {
-      const float csc = __fmul_rn(sc, s.tp[d][0]);
-      const bool me = lane == (nf & 31);
-      const int cj = nf >> 5;
-      put<kSlots>(f_sc, cj, csc, me); put<kSlots>(f_psc, cj, sc, me);
-      put<kSlots>(f_dpr, cj, pack_dpr(d + 1, row, 0), me);
-      put<kSlots>(f_w0, cj, w0, me);
-      put<kSlots>(f_w1, cj, w1, me); put<kSlots>(f_pm, cj, m, me);
-      put<kSlots>(f_key, cj, score_key(csc), me);
-      ++nf;
+    int p1 = gt1, p2 = gt2;
+    if (ge1 != gt1 || ge2 != gt2) {
+      uint64_t s0 = t_w0, s1 = t_w1;
+      tuple_add(s0, s1, d - 1, 1ull);
+      p1 = 0;
+      p2 = 0;
+#pragma unroll
+      for (int j = 0; j < kSlots; ++j) {
+        const bool v = lane + 32 * j < nl;
+        const int ed = l_dpr[j] & 0xff, ep = (l_dpr[j] >> 8) & 0xff, er = l_dpr[j] >> 16;
+        uint64_t e0 = s.r_w0[ep], e1 = s.r_w1[ep];
+        tuple_add(e0, e1, ed - 1, (uint64_t)er);
+        p1 += __popc(__ballot_sync(kFull, v && precedes(l_sc[j], ed, e0, e1, c1, d, s0, s1)));
+        p2 += __popc(__ballot_sync(kFull, v && precedes(l_sc[j], ed, e0, e1, c2, d + 1, t_w0, t_w1)));
+      }
     }
+    // places in L' = L with the candidates merged in
+    int P1 = kNone, P2 = kNone;
+    if (sib && child) {
+      if (c1 >= c2) { P1 = p1; P2 = p2 + 1; }
+      else { P2 = p2; P1 = p1 + 1; }
+    } else if (sib) {
+      P1 = p1;
+    } else if (child) {
+      P2 = p2;
+    }
+    // the next best entry is L'[0]; the new L[j] is L'[j + 1], a candidate
+    // or L[j + 1 - (candidates placed before it)]
+    float g_sc[kSlots];
+    int32_t g_dpr[kSlots];
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j) {
+      const int i = lane + 32 * j + 1;
+      const int src = i - (P1 < i ? 1 : 0) - (P2 < i ? 1 : 0);
+      const int sl = src & 31, sj = src >> 5;
+      float vs = __shfl_sync(kFull, l_sc[0], sl);
+      int32_t vd = __shfl_sync(kFull, l_dpr[0], sl);
+#pragma unroll
+      for (int jj = 1; jj < kSlots; ++jj) {
+        const float a = __shfl_sync(kFull, l_sc[jj], sl);
+        const int32_t ad = __shfl_sync(kFull, l_dpr[jj], sl);
+        if (sj == jj) { vs = a; vd = ad; }
+      }
+      if (i == P1) { vs = c1; vd = c1_dpr; }
+      else if (i == P2) { vs = c2; vd = c2_dpr; }
+      g_sc[j] = vs;
+      g_dpr[j] = vd;
+    }
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j) { l_sc[j] = g_sc[j]; l_dpr[j] = g_dpr[j]; }
+    if (P1 == 0) { t_sc = c1; t_dpr = c1_dpr; }
+    else if (P2 == 0) { t_sc = c2; t_dpr = c2_dpr; }
+    else { t_sc = h_sc; t_dpr = h_dpr; }
+    nl += (sib ? 1 : 0) + (child ? 1 : 0) - 1;
   }
   __syncwarp();
 
