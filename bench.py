@@ -313,8 +313,8 @@ CALL_SOURCES = {
     "build_conditioned": ["tsd_tree_cond.cu", "tsd_common.cuh"],
     "verify": ["tsd_verify.cu", "tsd_verify_tc.cu", "tsd_verify_mla.cu", "tsd_verify_mma.cu",
                "tsd_verify.cuh", "tsd_tcgen05.cuh", "tsd_common.cuh"],
-    "accept": ["tsd_accept.cu", "tsd_scan.cuh", "tsd_common.cuh"],
-    "commit": ["tsd_commit.cu", "tsd_common.cuh"],
+    "accept": ["tsd_accept.cu", "tsd_scan.cuh", "tsd_commit.cuh", "tsd_common.cuh"],
+    "commit": ["tsd_commit.cu", "tsd_commit.cuh", "tsd_common.cuh"],
 }
 
 
@@ -398,8 +398,8 @@ def run_ours(args, dist, config=None, lite=False):
     median_ms = statistics.median(step_ms)
 
     # ---- timed region B: per-call durations (eager) ----
-    calls = ["build", "verify", "accept", "commit"]
-    evc = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    calls = ["build", "verify", "accept", "commit", None, "accept_commit"]
+    evc = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     with torch.cuda.stream(stream):
         for i in range(args.steps):
             prep()
@@ -413,9 +413,15 @@ def run_ours(args, dist, config=None, lite=False):
             e[3].record(stream)
             step.commit(d["kt"], d["vt"], d["kc"], d["vc"], d["plen"], stream)
             e[4].record(stream)
+            # the same walk and commit as one call (tsd_accept_commit), from
+            # the same state
+            prep()
+            e[5].record(stream)
+            step.accept_commit(d["tl"], d["kt"], d["vt"], d["kc"], d["vc"], d["plen"], stream)
+            e[6].record(stream)
     torch.cuda.synchronize(dev)
     per_call = {c: statistics.mean(evc[i][j].elapsed_time(evc[i][j + 1]) for i in range(args.steps))
-                for j, c in enumerate(calls)}
+                for j, c in enumerate(calls) if c is not None}
     err_word = int(step.err[0].item())
 
     e2e = adaptive = paged = None
@@ -441,7 +447,8 @@ def run_ours(args, dist, config=None, lite=False):
     if traffic and traffic.get("digest") == source_digest(CALL_SOURCES[dominant]):
         traffic_val = traffic.get("bytes_per_launch")
     n_verify_kernels = 2 if step.ws_verify.numel() > 16 else 1
-    launches_per_step = 2 + n_verify_kernels + 2 + 1
+    # build: top-k scan + tree; verify; accept + commit: argmax scan + walk (which commits)
+    launches_per_step = 2 + n_verify_kernels + 2
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "nodes/s",
@@ -643,8 +650,8 @@ def run_e2e(args, step, host, d, dev, stream, plen0):
             step.verify(dbuf["q"], d["kc"], d["vc"], dbuf["plen"], dbuf["kt"], dbuf.get("vt"),
                         stream)
             need("accept")
-            step.accept(dbuf["tl"], stream)
-            step.commit(dbuf["kt"], dbuf.get("vt"), d["kc"], d["vc"], dbuf["plen"], stream)
+            step.accept_commit(dbuf["tl"], dbuf["kt"], dbuf.get("vt"), d["kc"], d["vc"],
+                               dbuf["plen"], stream)
             for o, r in zip(outs, res):
                 o.copy_(r, non_blocking=True)
             b.record(stream)

@@ -11,6 +11,7 @@
  *   tsd_accept_walk       target argmax per node, greedy walk to the accepted
  *                         path, bonus (correction) token, chain id
  *   tsd_commit_path       copy the accepted path's scratch KV into the cache
+ *   tsd_accept_commit     the walk and the commit in one call
  *
  * Sources of the operations (web pages, by title and section):
  *   "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4 for
@@ -369,6 +370,35 @@ tsd_status tsd_accept_walk_static(const float* logits, int B, int D, int S, int 
                                   int32_t* accept_rows, int32_t* bonus,
                                   int32_t* chain_id, int32_t* err,
                                   tsd_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * tsd_accept_commit
+ *
+ * tsd_accept_walk followed by the commit of its accepted paths
+ * (tsd_commit_path, or tsd_commit_path_paged when page_size > 0), in one call
+ * and one kernel per request after the argmax scan: the walk's CTA copies the
+ * path it found (V4 review, toy steps 5-6 and "Secret weapon").  Arguments are
+ * those of the two calls: the walk's (logits .. chain_id, ws, err, stream),
+ * then the commit's (desc, ktree, vtree, kcache / kpool, vcache / vpool,
+ * page_table, max_pages, page_size, num_pages, prefix_len), with page_size = 0
+ * (page_table NULL, max_pages and num_pages 0) for the contiguous cache.
+ * desc->B must equal B and desc->R must equal D + 1.  accept_len and
+ * accept_rows are written as by tsd_accept_walk (the commit does not read them
+ * back).  Outputs, error codes and the cache contents are identical to the two
+ * calls made in order.
+ * ws: tsd_accept_walk_workspace_size(B, D, V) bytes.
+ * -------------------------------------------------------------------------- */
+tsd_status tsd_accept_commit(const float* logits, int B, int D, int S, int V,
+                             const int32_t* token, const int32_t* parent,
+                             const uint64_t* mask, const uint8_t* is_leaf,
+                             int32_t* tgt, int32_t* accept_len,
+                             int32_t* accept_rows, int32_t* bonus,
+                             int32_t* chain_id, const tsd_attn_desc* desc,
+                             const void* ktree, const void* vtree, void* kcache,
+                             void* vcache, const int32_t* page_table, int max_pages,
+                             int page_size, int num_pages, int32_t* prefix_len,
+                             void* ws, size_t ws_bytes, int32_t* err,
+                             tsd_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * tsd_commit_path

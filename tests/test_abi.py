@@ -124,6 +124,25 @@ def test_commit_rejects(args):
     assert st == T.TSD_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("args", [dict(), dict(B=3), dict(D=5), dict(S=0), dict(S=17),
+                                  dict(logits=N), dict(ws_bytes=0), dict(kt=N), dict(kc=U),
+                                  dict(plen=N), dict(page_size=-1), dict(page_size=128),
+                                  dict(page_size=128, max_pages=1, table=A, num_pages=4)])
+def test_accept_commit_rejects(args):
+    """The walk's checks, the commit's, and the two agreeing on (B, D + 1)."""
+    kw = dict(B=2, D=4, S=3, V=32, logits=A, ws_bytes=1 << 20, kt=A, kc=A, plen=A,
+              table=N, max_pages=0, page_size=0, num_pages=0, dk=128)
+    kw.update(args)
+    d = _desc(dk=kw["dk"], dv=kw["dk"], cap=64)
+    if not args:
+        d.R = 9     # desc R != D + 1
+    st = T.lib.tsd_accept_commit(kw["logits"], kw["B"], kw["D"], kw["S"], kw["V"], A, A, A, A, N,
+                                 A, A, A, A, ctypes.byref(d), kw["kt"], A, kw["kc"], A,
+                                 kw["table"], kw["max_pages"], kw["page_size"], kw["num_pages"],
+                                 kw["plen"], A, kw["ws_bytes"], N, N)
+    assert st == T.TSD_ERR_INVALID_ARG
+
+
 def test_workspace_sizes_are_deterministic_and_scale():
     a = T.tsd_tree_build_workspace_size(32, 7, 151936, 8)
     assert a == T.tsd_tree_build_workspace_size(32, 7, 151936, 8) and a > 0

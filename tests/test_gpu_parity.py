@@ -1065,6 +1065,69 @@ def test_paged_commit_equals_contiguous(name):
         assert torch.equal(_gather(gp[3].cpu(), table, page_size), gc[3].cpu())
 
 
+@pytest.mark.parametrize("name,over", [("qwen", {}), ("batched", dict(B=6, V=20000)),
+                                       ("mla", dict(B=3, P=700, P_min=700, V=9000)),
+                                       ("long", dict(B=2, P=2000, P_min=2000, V=7000))])
+@pytest.mark.parametrize("paged", [False, True])
+def test_accept_commit_matches_oracle_walk_and_commit(name, over, paged):
+    """tsd_accept_commit (the walk's kernel commits the path) against the
+    oracle's walk and commit; one request is placed so that its accepted path
+    overflows the cache (skipped, TSD_DEV_ERR_CAPACITY)."""
+    d = inputs(name, **over)
+    w, tree = d["w"], d["tree"]
+    page_size = 128
+    cap = -(-w.cap // page_size) * page_size if paged else w.cap
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    kc = torch.nn.functional.pad(kc, (0, 0, 0, cap - kc.shape[2]))
+    vc = None if vc is None else torch.nn.functional.pad(vc, (0, 0, 0, cap - vc.shape[2]))
+    tl = W.target_logits(w, torch.from_numpy(tree["depth"]), d["logits"])
+    tgt = oracle.argmax(tl.numpy())
+    ref = oracle.accept_walk(tgt, tree, w.S)
+    over_b = [b for b in range(w.B) if ref["accept_len"][b] > 0]
+    if over_b:   # the last request with a non-empty path no longer fits
+        b = over_b[-1]
+        plen[b] = cap - int(ref["accept_len"][b])
+    kc_ref = W.bits(kc).copy()
+    vc_ref = None if vc is None else W.bits(vc).copy()
+    pl_ref = plen.numpy().copy()
+    # the oracle commit checks against the cache length it is handed
+    skipped = oracle.commit(W.bits(kt), None if vt is None else W.bits(vt), ref["accept_rows"],
+                            ref["accept_len"], kc_ref, vc_ref, pl_ref, w.S,
+                            v_aliases_k=w.v_aliases_k)
+    assert skipped == (1 if over_b else 0)
+
+    step = TreeVerifyStep(w.B, w.S, w.V, w.k, w.D, w.Hq, w.Hkv, w.dk, w.dv, cap, w.torch_dtype,
+                          w.v_aliases_k, w.scale, DEV)
+    set_tree(step, tree)
+    gtl, gkt, gvt, gpl = gpu(tl, kt, vt, plen)
+    if paged:
+        kpool, table = _paged(kc, page_size, seed=5)
+        vpool = None if vc is None else _paged(vc, page_size, seed=5)[0]
+        gk, gv, gtab = gpu(kpool, vpool, table)
+    else:
+        gk, gv = gpu(kc, vc)
+        gtab = None
+    t, wk = step.tree, step.walk
+    T.tsd_accept_commit(gtl, w.S, t.token, t.parent, t.mask, t.is_leaf, wk.tgt, wk.accept_len,
+                        wk.accept_rows, wk.bonus, wk.chain_id, step.desc, gkt, gvt, gk, gv, gpl,
+                        step.ws_walk, step.err, page_table=gtab, page_size=page_size if paged else 0)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(wk.tgt.cpu().numpy(), tgt)
+    for key in ("accept_len", "accept_rows", "bonus", "chain_id"):
+        np.testing.assert_array_equal(getattr(wk, key).cpu().numpy(), ref[key])
+    gk_c = _gather(gk.cpu(), table, page_size) if paged else gk.cpu()
+    np.testing.assert_array_equal(W.bits(gk_c), kc_ref)
+    if vc is not None:
+        gv_c = _gather(gv.cpu(), table, page_size) if paged else gv.cpu()
+        np.testing.assert_array_equal(W.bits(gv_c), vc_ref)
+    np.testing.assert_array_equal(gpl.cpu().numpy(), pl_ref)
+    err = int(step.err[0])
+    if over_b:
+        assert err & T.TSD_DEV_ERR_MASK == T.TSD_DEV_ERR_CAPACITY and err & 0xFFFFFF == over_b[-1]
+    else:
+        assert err == 0
+
+
 def test_paged_bad_page_is_reported_not_read():
     d = inputs("qwen", B=2, P=600, P_min=600, V=2000)
     w = d["w"]

@@ -17,6 +17,9 @@ Typical step on one stream::
     tsd_accept_walk(logits, S, tree..., walk..., ws_walk, err)
     tsd_commit_path(desc, S, ktree, vtree, walk.accept_rows, walk.accept_len,
                     kcache, vcache, prefix_len, err)
+
+or the last two as one call, ``tsd_accept_commit`` (the walk's kernel commits
+the path it finds).
 """
 
 from __future__ import annotations
@@ -51,7 +54,8 @@ EXPORTED = ("tsd_status_string", "tsd_version", "tsd_tree_build_workspace_size",
             "tsd_verify_workspace_size",
             "tsd_tree_verify_attn", "tsd_tree_verify_attn_paged", "tsd_commit_path_paged",
             "tsd_accept_walk_workspace_size", "tsd_accept_walk", "tsd_accept_walk_static",
-            "tsd_commit_path", "tsd_set_verify_path", "tsd_set_wait_budget")
+            "tsd_commit_path", "tsd_accept_commit", "tsd_set_verify_path",
+            "tsd_set_wait_budget")
 
 
 class TsdError(RuntimeError):
@@ -103,6 +107,10 @@ def _load():
     lib.tsd_commit_path_paged.argtypes = [ctypes.POINTER(tsd_attn_desc), I, P, P, P, P, P, P, P, I,
                                           I, I, P, P, P]
     lib.tsd_commit_path_paged.restype = I
+    lib.tsd_accept_commit.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, P,
+                                      ctypes.POINTER(tsd_attn_desc), P, P, P, P, P, I, I, I, P,
+                                      P, Z, P, P]
+    lib.tsd_accept_commit.restype = I
     lib.tsd_set_verify_path.argtypes = [I]
     lib.tsd_set_verify_path.restype = I
     lib.tsd_set_wait_budget.argtypes = [ctypes.c_longlong]
@@ -396,3 +404,32 @@ def tsd_commit_path(desc, S, ktree, vtree, accept_rows, accept_len, kcache, vcac
     pvc = None if d.v_aliases_k else _t(vcache, "vcache", dt, (d.B, d.Hkv, d.cap, d.dv))
     _check("tsd_commit_path", _L().tsd_commit_path(
         ctypes.byref(d), S, pkt, pvt, par, pal, pkc, pvc, ppl, _err(err), _stream(stream)))
+
+
+def tsd_accept_commit(logits, S, token, parent, mask, is_leaf, tgt, accept_len, accept_rows,
+                      bonus, chain_id, desc, ktree, vtree, kcache, vcache, prefix_len, ws,
+                      err=None, stream=None, page_table=None, page_size=0):
+    """tsd_accept_walk, then the commit of the accepted paths, in one call.
+
+    kcache/vcache are the contiguous cache, or with ``page_table`` [B][max_pages]
+    the page pools [num_pages][Hkv][page_size][d] of tsd_commit_path_paged.
+    """
+    d = desc
+    dt = _attn_dtype(d)
+    walk = _walk_args(logits, S, token, parent, mask, is_leaf, tgt, accept_len, accept_rows,
+                      bonus, chain_id)
+    if walk[1] != d.B or walk[2] + 1 != d.R:
+        raise ValueError("tsd_accept_commit: logits batch / rows do not match desc (B, R)")
+    pkt, pvt, _, _, ppl = _commit_common(d, S, ktree, vtree, accept_rows, accept_len, prefix_len)
+    if page_table is None:
+        pkc = _t(kcache, "kcache", dt, (d.B, d.Hkv, d.cap, d.dk))
+        pvc = None if d.v_aliases_k else _t(vcache, "vcache", dt, (d.B, d.Hkv, d.cap, d.dv))
+        paging = (None, 0, 0, 0)
+    else:
+        npg, mp = kcache.shape[0], page_table.shape[1]
+        pkc = _t(kcache, "kpool", dt, (npg, d.Hkv, page_size, d.dk))
+        pvc = None if d.v_aliases_k else _t(vcache, "vpool", dt, (npg, d.Hkv, page_size, d.dv))
+        paging = (_t(page_table, "page_table", _I32, (d.B, mp)), mp, page_size, npg)
+    _check("tsd_accept_commit", _L().tsd_accept_commit(
+        *walk, ctypes.byref(d), pkt, pvt, pkc, pvc, *paging, ppl, _ptr(ws), _nbytes(ws),
+        _err(err), _stream(stream)))

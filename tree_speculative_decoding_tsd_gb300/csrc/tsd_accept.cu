@@ -11,10 +11,14 @@
 //
 // K4 vocab_scan_kernel<true>: per-chunk argmax of every target-logit row
 //    (HBM-bound scan; ties go to the lowest id).
-// K5 accept_walk_kernel: one warp per request.  Merges the chunk maxima into
-//    tgt[r], checks the tree, walks: at row u, the child c (parent[c] == u)
-//    with token[c] == tgt[u] is accepted (lowest row if several), until no
-//    child matches.
+// K5 accept_walk_kernel: one CTA per request.  Merges the chunk maxima into
+//    tgt[r], checks the tree, walks (one warp): at row u, the child c
+//    (parent[c] == u) with token[c] == tgt[u] is accepted (lowest row if
+//    several), until no child matches.  In tsd_accept_commit the same CTA then
+//    commits the accepted path (the commit of tsd_commit_path, with the path
+//    taken from shared memory); its scratch-pad K/V rows were prefetched into
+//    L2 at the kernel's start, so the copy reads L2.
+#include "tsd_commit.cuh"
 #include "tsd_common.cuh"
 #include "tsd_host.h"
 #include "tsd_scan.cuh"
@@ -30,20 +34,34 @@ constexpr int kMaxR = 65;
 
 constexpr int kWalkWarps = 32;   // one warp per tree row up to 32 rows: their chunk loads overlap
 
+template <bool kCommit>
 __global__ void __launch_bounds__(32 * kWalkWarps)
 accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
                    const int32_t* __restrict__ token, const int32_t* __restrict__ parent,
                    const uint64_t* __restrict__ mask, const uint8_t* __restrict__ is_leaf,
                    int32_t* __restrict__ tgt_out, int32_t* __restrict__ accept_len,
                    int32_t* __restrict__ accept_rows, int32_t* __restrict__ bonus,
-                   int32_t* __restrict__ chain_id, int32_t* __restrict__ err) {
-  grid_dependency_sync();
+                   int32_t* __restrict__ chain_id, int32_t* __restrict__ err, CommitArgs ca) {
   __shared__ int32_t s_tgt[kMaxR], s_tok[kMaxR], s_par[kMaxR];
   __shared__ uint64_t s_mask[kMaxR];
   __shared__ uint8_t s_leaf[kMaxR];
+  __shared__ int32_t s_path[kCommitMaxRows];
+  __shared__ int s_P, s_L;
+  __shared__ CommitSmem s_commit;
   const int b = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long o = (long)b * R;
+  if (kCommit) {
+    // the request's scratch-pad K/V rows into L2 (a hint, before the wait)
+    const long kbytes = (long)R * ca.Hkv * ca.krow, vbytes = (long)R * ca.Hkv * ca.vrow;
+    if (threadIdx.x == 0) prefetch_l2(ca.ktree + b * kbytes, kbytes);
+    if (threadIdx.x == 32 && vbytes > 0) prefetch_l2(ca.vtree + b * vbytes, vbytes);
+  }
+  grid_dependency_sync();
+  if (kCommit && threadIdx.x == 0) {
+    s_P = ca.prefix_len[b];
+    s_commit.code = kNoError;
+  }
 
   // tree metadata, then tgt[r]: the largest of the row's chunk maxima.  Warp
   // w takes rows w, w+32, ...; its lanes split the (at most 256) chunks and
@@ -73,57 +91,67 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
     }
   }
   __syncthreads();
-  if (warp != 0) return;
-  bool bad = false;
-  for (int r = lane; r < R; r += 32) {
-    const int32_t p = s_par[r];
-    if (r > 0 && (p < 0 || p >= r)) bad = true;
-  }
-  bad = __any_sync(kFull, bad);
-  __syncwarp();
+  if (warp == 0) {
+    bool bad = false;
+    for (int r = lane; r < R; r += 32) {
+      const int32_t p = s_par[r];
+      if (r > 0 && (p < 0 || p >= r)) bad = true;
+    }
+    bad = __any_sync(kFull, bad);
+    __syncwarp();
 
-  int32_t* rows = accept_rows + (long)b * (S + 1);
-  int u = 0, L = 0;
-  if (!bad) {
-    for (;;) {
-      const int want = s_tgt[u];
-      int found = R;  // lowest matching child row
-      for (int base = 1; base < R; base += 32) {
-        const int c = base + lane;
-        const bool hit = c < R && s_par[c] == u && s_tok[c] == want;
-        const unsigned bal = __ballot_sync(kFull, hit);
-        if (bal && found == R) found = base + __ffs(bal) - 1;
+    int32_t* rows = accept_rows + (long)b * (S + 1);
+    int u = 0, L = 0;
+    if (!bad) {
+      for (;;) {
+        const int want = s_tgt[u];
+        int found = R;  // lowest matching child row
+        for (int base = 1; base < R; base += 32) {
+          const int c = base + lane;
+          const bool hit = c < R && s_par[c] == u && s_tok[c] == want;
+          const unsigned bal = __ballot_sync(kFull, hit);
+          if (bal && found == R) found = base + __ffs(bal) - 1;
+        }
+        if (found == R) break;
+        if (L == S) { bad = true; break; }
+        ++L;
+        if (lane == 0) {
+          rows[L] = found;
+          s_path[L] = found;
+        }
+        u = found;
       }
-      if (found == R) break;
-      if (L == S) { bad = true; break; }
-      ++L;
-      if (lane == 0) rows[L] = found;
-      u = found;
     }
-  }
-  if (bad) {
-    if (lane == 0) report_error(err, TSD_DEV_ERR_BAD_TREE, b);
-    u = 0;
-    L = 0;
-  }
-  __syncwarp();
-  for (int i = lane; i <= S; i += 32)
-    if (i == 0) rows[0] = 0;
-    else if (i > L) rows[i] = -1;
+    if (bad) {
+      if (lane == 0) report_error(err, TSD_DEV_ERR_BAD_TREE, b);
+      u = 0;
+      L = 0;
+    }
+    __syncwarp();
+    for (int i = lane; i <= S; i += 32)
+      if (i == 0) rows[0] = s_path[0] = 0;
+      else if (i > L) rows[i] = s_path[i] = -1;
 
-  int chain = -1;
-  if (L > 0) {
-    for (int base = 1; base < R && chain < 0; base += 32) {
-      const int c = base + lane;
-      const bool hit = c < R && s_leaf[c] && ((s_mask[c] >> (u - 1)) & 1ull);
-      const unsigned bal = __ballot_sync(kFull, hit);
-      if (bal) chain = base + __ffs(bal) - 1;
+    int chain = -1;
+    if (L > 0) {
+      for (int base = 1; base < R && chain < 0; base += 32) {
+        const int c = base + lane;
+        const bool hit = c < R && s_leaf[c] && ((s_mask[c] >> (u - 1)) & 1ull);
+        const unsigned bal = __ballot_sync(kFull, hit);
+        if (bal) chain = base + __ffs(bal) - 1;
+      }
     }
-  }
-  if (lane == 0) {
-    accept_len[b] = L;
-    bonus[b] = s_tgt[u];
-    chain_id[b] = chain;
+    if (lane == 0) {
+      accept_len[b] = L;
+      bonus[b] = s_tgt[u];
+      chain_id[b] = chain;
+      s_L = L;
+    }
+  }  // warp 0
+  if (kCommit) {
+    __syncthreads();
+    const int r_tid = threadIdx.x <= S ? s_path[threadIdx.x] : 0;
+    commit_request<32 * kWalkWarps>(ca, s_commit, b, s_P, s_L, r_tid);
   }
 }
 
@@ -162,8 +190,48 @@ extern "C" tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, 
   uint64_t* part = (uint64_t*)ws;
   launch(vocab_scan_kernel<true>, dim3((unsigned)(rows * g.nchunk)), dim3(kScanThreads), 0, st,
       logits, V, 1, g.nchunk, g.chunk_len, part, g.one_wave, nullptr, 1);
-  launch(accept_walk_kernel, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk, token,
-      parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err);
+  launch(accept_walk_kernel<false>, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk,
+      token, parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err,
+      CommitArgs{});
+  return cuda_status();
+}
+
+extern "C" tsd_status tsd_accept_commit(const float* logits, int B, int D, int S, int V,
+                                        const int32_t* token, const int32_t* parent,
+                                        const uint64_t* mask, const uint8_t* is_leaf,
+                                        int32_t* tgt, int32_t* accept_len, int32_t* accept_rows,
+                                        int32_t* bonus, int32_t* chain_id,
+                                        const tsd_attn_desc* desc, const void* ktree,
+                                        const void* vtree, void* kcache, void* vcache,
+                                        const int32_t* page_table, int max_pages, int page_size,
+                                        int num_pages, int32_t* prefix_len, void* ws,
+                                        size_t ws_bytes, int32_t* err, tsd_stream_t stream) {
+  if (B < 1 || D < 1 || D > kMaxR - 1 || S < 1 || S > 16 || V < 1 || V > (1 << 30))
+    return TSD_ERR_INVALID_ARG;
+  if ((long)B * (D + 1) > (1l << 24)) return TSD_ERR_INVALID_ARG;
+  if (!ok_ptr(logits) || !ok_ptr(token) || !ok_ptr(parent) || !ok_ptr(mask) ||
+      !ok_ptr(is_leaf) || !ok_opt_ptr(tgt) || !ok_ptr(accept_len) || !ok_ptr(accept_rows) ||
+      !ok_ptr(bonus) || !ok_ptr(chain_id) || !ok_opt_ptr(err))
+    return TSD_ERR_INVALID_ARG;
+  if (desc == nullptr || desc->B != B || desc->R != D + 1 || page_size < 0)
+    return TSD_ERR_INVALID_ARG;
+  CommitArgs ca;
+  const tsd_status cst = commit_args(desc, S, ktree, vtree, accept_rows, accept_len, kcache,
+                                     vcache, page_table, max_pages, page_size, num_pages,
+                                     prefix_len, err, &ca);
+  if (cst != TSD_OK) return cst;
+  const size_t need = tsd_accept_walk_workspace_size(B, D, V);
+  if (ws_bytes < need || !ok_ptr(ws)) return TSD_ERR_INVALID_ARG;
+
+  const cudaStream_t st = (cudaStream_t)stream;
+  const int R = D + 1;
+  const long rows = (long)B * R;
+  const ScanGeom g = scan_geometry(rows, V, 1, true);
+  uint64_t* part = (uint64_t*)ws;
+  launch(vocab_scan_kernel<true>, dim3((unsigned)(rows * g.nchunk)), dim3(kScanThreads), 0, st,
+      logits, V, 1, g.nchunk, g.chunk_len, part, g.one_wave, nullptr, 1);
+  launch(accept_walk_kernel<true>, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk,
+      token, parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err, ca);
   return cuda_status();
 }
 
@@ -258,7 +326,8 @@ extern "C" tsd_status tsd_accept_walk_static(const float* logits, int B, int D, 
   const ScanGeom g = scan_geometry(rows, V, 1, true);
   launch(vocab_scan_kernel<true>, dim3((unsigned)(rows * g.nchunk)), dim3(kScanThreads), 0, st,
       logits, V, 1, g.nchunk, g.chunk_len, part, g.one_wave, nullptr, 1);
-  launch(accept_walk_kernel, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk, token,
-      parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err);
+  launch(accept_walk_kernel<false>, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk,
+      token, parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err,
+      CommitArgs{});
   return cuda_status();
 }

@@ -12,7 +12,8 @@ import dataclasses
 
 import torch
 
-from . import (make_desc, tsd_accept_walk, tsd_accept_walk_workspace_size, tsd_commit_path,
+from . import (make_desc, tsd_accept_commit, tsd_accept_walk, tsd_accept_walk_workspace_size,
+               tsd_commit_path,
                tsd_tree_build, tsd_tree_build_adaptive, tsd_tree_build_conditioned,
                tsd_tree_build_workspace_size, tsd_tree_verify_attn, tsd_verify_workspace_size,
                workspace)
@@ -102,9 +103,16 @@ class TreeVerifyStep:
         tsd_commit_path(self.desc, self.S, ktree, vtree, w.accept_rows, w.accept_len, kcache,
                         vcache, prefix_len, self.err, stream)
 
+    def accept_commit(self, logits, ktree, vtree, kcache, vcache, prefix_len, stream=None):
+        """accept() then commit() as one call (the walk's kernel commits the path)."""
+        t, w = self.tree, self.walk
+        tsd_accept_commit(logits, self.S, t.token, t.parent, t.mask, t.is_leaf, w.tgt,
+                          w.accept_len, w.accept_rows, w.bonus, w.chain_id, self.desc, ktree,
+                          vtree, kcache, vcache, prefix_len, self.ws_walk, self.err, stream)
+
     def run(self, probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits,
             stream=None):
-        """The whole step: build -> verify -> accept -> commit (asynchronous)."""
+        """The whole step: build -> verify -> accept + commit (asynchronous)."""
         self._round(probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits, None,
                     None, stream)
 
@@ -143,8 +151,7 @@ class TreeVerifyStep:
         else:
             self.build_adaptive(probs, root_tok, cost_d, cost_v, stream)
         self.verify(q, kcache, vcache, prefix_len, ktree, vtree, stream)
-        self.accept(logits, stream)
-        self.commit(ktree, vtree, kcache, vcache, prefix_len, stream)
+        self.accept_commit(logits, ktree, vtree, kcache, vcache, prefix_len, stream)
 
     @classmethod
     def for_workload(cls, w, device="cuda"):
