@@ -38,13 +38,11 @@ struct TreeSmem {
   int32_t ti[kMaxS][kMaxK];   // top-k token ids per position
   float cost[kMaxD + 1];      // adaptive mode: C_d + C_v(n), n = 0..D
   // the tree's rows, written as they are popped (by every lane of the
-  // popping warp, so that each lane reads back only its own writes)
+  // popping warp, so that each lane reads back only its own writes): score,
+  // ancestor mask, and the popped entry (depth | parent row << 8 | rank << 16)
   uint64_t r_mask[kMaxD + 1];
-  uint64_t r_w0[kMaxD + 1], r_w1[kMaxD + 1];   // rank tuples
   float r_sc[kMaxD + 1];
-  int32_t r_par[kMaxD + 1];
-  int32_t r_tok[kMaxD + 1];
-  int32_t r_dep[kMaxD + 1];
+  int32_t r_dpr[kMaxD + 1];
   uint8_t has_child[kMaxD + 1];
 };
 
@@ -57,6 +55,21 @@ __device__ __forceinline__ void tuple_add(uint64_t& w0, uint64_t& w1, int level,
 
 // Depth, parent row and rank of a frontier entry in one word (each < 256).
 __device__ __forceinline__ int pack_dpr(int d, int par, int rk) { return d | (par << 8) | (rk << 16); }
+
+// Rank tuple of the entry dpr: its rank at its depth, then its ancestors'
+// ranks, read from the popped rows (a parent row precedes its children, so
+// the walk reaches the root in at most depth steps).
+__device__ __forceinline__ void entry_tuple(const TreeSmem& s, int32_t dpr, uint64_t& w0,
+                                            uint64_t& w1) {
+  w0 = 0ull;
+  w1 = 0ull;
+  for (int it = 0; it < kMaxS; ++it) {
+    const int d = dpr & 0xff, par = (dpr >> 8) & 0xff;
+    tuple_add(w0, w1, d - 1, (uint64_t)(dpr >> 16));
+    if (par == 0) break;
+    dpr = s.r_dpr[par];
+  }
+}
 
 // Full order between two frontier entries (score desc, depth asc, tuple asc).
 __device__ __forceinline__ bool precedes(float sa, int da, uint64_t a0, uint64_t a1, float sb,
@@ -119,8 +132,8 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
 
   // ---- the pops: one warp, rows in shared memory ----
   // An entry is (score, depth | parent row << 8 | rank << 16).  Its rank
-  // tuple is its parent row's tuple with its rank added at its depth, so the
-  // tuple is looked up (rows keep theirs) only where scores tie.  The best
+  // tuple follows from its own and its ancestors' entries, so it is only
+  // built where scores tie.  The best
   // entry not yet popped (t_*) is held by every lane; the rest of the
   // frontier is the sorted list L (l_*).  A pop's sibling and child go to
   // the places given by the count of L's entries before them (ballots: L is
@@ -131,8 +144,9 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
 #pragma unroll
   for (int j = 0; j < kSlots; ++j) { l_sc[j] = 0.f; l_dpr[j] = pack_dpr(1, 0, 0); }
   // row 0 = root
-  s.r_sc[0] = 1.0f; s.r_par[0] = -1; s.r_tok[0] = __shfl_sync(kFull, root, 0);
-  s.r_dep[0] = 0; s.r_mask[0] = 0ull; s.r_w0[0] = 0ull; s.r_w1[0] = 0ull;
+  s.r_sc[0] = 1.0f;
+  s.r_mask[0] = 0ull;
+  s.r_dpr[0] = 0;
   // the first entry: rank 0 at depth 1
   float t_sc = __fmul_rn(1.0f, s.tp[0][0]);
   int32_t t_dpr = pack_dpr(1, 0, 0);
@@ -152,8 +166,6 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
     const float q_sib = s.tp[d - 1][sib ? rk + 1 : rk];
     const float q_child = s.tp[child ? d : d - 1][0];
     const uint64_t pm = s.r_mask[par];
-    uint64_t t_w0 = s.r_w0[par], t_w1 = s.r_w1[par];
-    const int32_t tok = s.ti[d - 1][rk];
     const float h_sc = __shfl_sync(kFull, l_sc[0], 0);     // L[0]
     const int32_t h_dpr = __shfl_sync(kFull, l_dpr[0], 0);
     if (adaptive) {
@@ -164,14 +176,9 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       }
       acc = acc1;
     }
-    tuple_add(t_w0, t_w1, d - 1, (uint64_t)rk);
     s.r_sc[row] = t_sc;
-    s.r_par[row] = par;
-    s.r_tok[row] = tok;
-    s.r_dep[row] = d;
+    s.r_dpr[row] = t_dpr;
     s.r_mask[row] = pm | (1ull << (row - 1));
-    s.r_w0[row] = t_w0;
-    s.r_w1[row] = t_w1;
     // nothing is popped after the last row: no new entries
     if (row == D) break;
 
@@ -192,6 +199,9 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
     }
     int p1 = gt1, p2 = gt2;
     if (ge1 != gt1 || ge2 != gt2) {
+      // the child's tuple is the popped entry's; the sibling's is one more at depth d
+      uint64_t t_w0, t_w1;
+      entry_tuple(s, t_dpr, t_w0, t_w1);
       uint64_t s0 = t_w0, s1 = t_w1;
       tuple_add(s0, s1, d - 1, 1ull);
       p1 = 0;
@@ -199,9 +209,9 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
 #pragma unroll
       for (int j = 0; j < kSlots; ++j) {
         const bool v = lane + 32 * j < nl;
-        const int ed = l_dpr[j] & 0xff, ep = (l_dpr[j] >> 8) & 0xff, er = l_dpr[j] >> 16;
-        uint64_t e0 = s.r_w0[ep], e1 = s.r_w1[ep];
-        tuple_add(e0, e1, ed - 1, (uint64_t)er);
+        const int ed = l_dpr[j] & 0xff;
+        uint64_t e0, e1;
+        entry_tuple(s, l_dpr[j], e0, e1);
         p1 += __popc(__ballot_sync(kFull, v && precedes(l_sc[j], ed, e0, e1, c1, d, s0, s1)));
         p2 += __popc(__ballot_sync(kFull, v && precedes(l_sc[j], ed, e0, e1, c2, d + 1, t_w0, t_w1)));
       }
@@ -253,13 +263,20 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   // leaf, so verify, walk and commit treat them as never accepted.
   for (int r = lane; r <= D; r += 32) s.has_child[r] = 0;
   __syncwarp();
-  for (int r = 1 + lane; r <= kept; r += 32) s.has_child[s.r_par[r]] = 1;
+  for (int r = 1 + lane; r <= kept; r += 32) s.has_child[(s.r_dpr[r] >> 8) & 0xff] = 1;
   __syncwarp();
   for (int r = lane; r <= D; r += 32) {
     if (r <= kept) {
-      token[o + r] = s.r_tok[r];
-      parent[o + r] = s.r_par[r];
-      depth[o + r] = s.r_dep[r];
+      const int32_t dpr = s.r_dpr[r];
+      const int d = dpr & 0xff;
+      if (r == 0) {
+        token[o] = root;
+        parent[o] = -1;
+      } else {
+        token[o + r] = s.ti[d - 1][dpr >> 16];
+        parent[o + r] = (dpr >> 8) & 0xff;
+      }
+      depth[o + r] = d;
       score[o + r] = s.r_sc[r];
       mask[o + r] = s.r_mask[r];
       is_leaf[o + r] = s.has_child[r] ? 0 : 1;
