@@ -110,20 +110,33 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 
 // Top-k of the 32*NC candidates held by the warp (NC per lane), returned as
 // a warp-distributed list (lane j holds the j-th largest, lanes >= k hold
-// whatever).  k rounds of a warp-wide maximum; the winner is removed from its
-// lane (candidates are distinct, so the winner is unique).  Missing
-// candidates are 0.  The lanes' arrays are consumed.
+// whatever).  Each lane first sorts its candidates in descending order (an
+// odd-even transposition network, NC phases); then k rounds take the warp
+// maximum of the lanes' first candidates, and the lane that held it (the
+// candidates are distinct, so there is one) moves up its next one.  A round
+// is two 32-bit reductions and one shift of the lane's list, instead of a
+// search through all NC candidates.  Missing candidates are 0.  The lanes'
+// arrays are consumed.
 template <int NC>
 __device__ __forceinline__ uint64_t warp_topk(uint64_t (&c)[NC], int k, int lane) {
+#pragma unroll
+  for (int ph = 0; ph < NC; ++ph) {
+#pragma unroll
+    for (int i = ph & 1; i + 1 < NC; i += 2) {
+      const uint64_t a = c[i], b = c[i + 1];
+      const bool sw = b > a;
+      c[i] = sw ? b : a;
+      c[i + 1] = sw ? a : b;
+    }
+  }
   uint64_t entry = 0ull;
   for (int r = 0; r < k; ++r) {
-    uint64_t m = 0ull;
-#pragma unroll
-    for (int i = 0; i < NC; ++i) m = c[i] > m ? c[i] : m;
-    const uint64_t w = warp_max_u64(m);
+    const uint64_t w = warp_max_u64(c[0]);
     if (lane == r) entry = w;
+    const bool mine = c[0] == w;
 #pragma unroll
-    for (int i = 0; i < NC; ++i) c[i] = (c[i] == w) ? 0ull : c[i];
+    for (int i = 0; i + 1 < NC; ++i) c[i] = mine ? c[i + 1] : c[i];
+    c[NC - 1] = mine ? 0ull : c[NC - 1];
   }
   return entry;
 }
