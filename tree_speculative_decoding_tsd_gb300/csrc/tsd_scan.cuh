@@ -260,32 +260,35 @@ vocab_scan_kernel(const float* __restrict__ x, int V, int k, int nchunk, int chu
     warp_list_offer(entry, thr, c, k, kmask, lane);
   }
 
-  // pass 2: the warp re-reads, one thread at a time, the elements of its
-  // threads whose maximum reaches T: lane j takes that thread's j-th float4
-  unsigned act = __ballot_sync(kFull, m >= cut);
-  while (act) {
-    const int t = warp * 32 + __ffs(act) - 1;
-    act &= act - 1;
-    const int cnt = t < nvec ? (nvec - t + kScanThreads - 1) / kScanThreads : 0;
-    for (int j0 = 0; j0 < cnt; j0 += 32) {
-      const int j = j0 + lane;
-      const bool have = j < cnt;
-      const float4 f = have ? __ldg(xv + t + j * kScanThreads) : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float e[4] = {f.x, f.y, f.z, f.w};
-      unsigned pend = 0;
+  // pass 2: the warp re-reads the elements of its threads whose maximum
+  // reaches T, all of them at once (one round trip per 32 float4s): item q
+  // is float4 q % cmax of the (q / cmax)-th such thread
+  const unsigned act = __ballot_sync(kFull, m >= cut);
+  const int cmax = (nvec + kScanThreads - 1) / kScanThreads;   // float4s per thread, at most
+  const int items = __popc(act) * cmax;
+  for (int q0 = 0; q0 < items; q0 += 32) {
+    const int q = q0 + lane;
+    int vi = nvec;   // the float4 of item q, or nvec for none
+    if (q < items) {
+      const int a = q / cmax;
+      vi = warp * 32 + (int)__fns(act, 0, a + 1) + (q - a * cmax) * kScanThreads;
+    }
+    const bool have = vi < nvec;
+    const float4 f = have ? __ldg(xv + vi) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float e[4] = {f.x, f.y, f.z, f.w};
+    unsigned pend = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) pend |= (have && e[i] >= cut) ? (1u << i) : 0u;
-      const uint32_t i0 = (uint32_t)(a0 + 4 * (t + j * kScanThreads));
-      while (__any_sync(kFull, pend != 0)) {
-        uint64_t cnd = 0ull;
-        if (pend) {
-          const int i = __ffs(pend) - 1;
-          pend &= pend - 1;
-          const float x = i == 0 ? e[0] : i == 1 ? e[1] : i == 2 ? e[2] : e[3];
-          cnd = make_cand(x, i0 + i);
-        }
-        warp_list_offer(entry, thr, cnd, k, kmask, lane);
+    for (int i = 0; i < 4; ++i) pend |= (have && e[i] >= cut) ? (1u << i) : 0u;
+    const uint32_t i0 = (uint32_t)(a0 + 4 * vi);
+    while (__any_sync(kFull, pend != 0)) {
+      uint64_t cnd = 0ull;
+      if (pend) {
+        const int i = __ffs(pend) - 1;
+        pend &= pend - 1;
+        const float x = i == 0 ? e[0] : i == 1 ? e[1] : i == 2 ? e[2] : e[3];
+        cnd = make_cand(x, i0 + i);
       }
+      warp_list_offer(entry, thr, cnd, k, kmask, lane);
     }
   }
 
