@@ -14,7 +14,8 @@
 // K5 accept_walk_kernel: one CTA per request.  Merges the chunk maxima into
 //    tgt[r], checks the tree, walks (one warp): at row u, the child c
 //    (parent[c] == u) with token[c] == tgt[u] is accepted (lowest row if
-//    several), until no child matches.  In tsd_accept_commit the same CTA then
+//    several), until no child matches.  Every row's accepted child is found
+//    first, in parallel, so the walk itself only follows them.  In tsd_accept_commit the same CTA then
 //    commits the accepted path (the commit of tsd_commit_path, with the path
 //    taken from shared memory); its scratch-pad K/V rows were prefetched into
 //    L2 at the kernel's start, so the copy reads L2.
@@ -46,6 +47,7 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
   __shared__ uint64_t s_mask[kMaxR];
   __shared__ uint8_t s_leaf[kMaxR];
   __shared__ int32_t s_path[kCommitMaxRows];
+  __shared__ int32_t s_child[kMaxR];
   __shared__ int s_P, s_L;
   __shared__ CommitSmem s_commit;
   const int b = blockIdx.x;
@@ -100,18 +102,23 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
     bad = __any_sync(kFull, bad);
     __syncwarp();
 
+    // the lowest matching child of every row u (parent[c] == u and token[c]
+    // == tgt[u]): each row c posts itself to its parent, so the walk below
+    // is one shared-memory read per level
+    for (int r = lane; r < R; r += 32) s_child[r] = R;
+    __syncwarp();
+    if (!bad)
+      for (int c = 1 + lane; c < R; c += 32) {
+        const int p = s_par[c];
+        if (s_tok[c] == s_tgt[p]) atomicMin(&s_child[p], c);
+      }
+    __syncwarp();
+
     int32_t* rows = accept_rows + (long)b * (S + 1);
     int u = 0, L = 0;
     if (!bad) {
       for (;;) {
-        const int want = s_tgt[u];
-        int found = R;  // lowest matching child row
-        for (int base = 1; base < R; base += 32) {
-          const int c = base + lane;
-          const bool hit = c < R && s_par[c] == u && s_tok[c] == want;
-          const unsigned bal = __ballot_sync(kFull, hit);
-          if (bal && found == R) found = base + __ffs(bal) - 1;
-        }
+        const int found = s_child[u];
         if (found == R) break;
         if (L == S) { bad = true; break; }
         ++L;
