@@ -14,8 +14,9 @@
 // K5 accept_walk_kernel: one CTA per request.  Merges the chunk maxima into
 //    tgt[r], checks the tree, walks (one warp): at row u, the child c
 //    (parent[c] == u) with token[c] == tgt[u] is accepted (lowest row if
-//    several), until no child matches.  Every row's accepted child is found
-//    first, in parallel, so the walk itself only follows them.  In tsd_accept_commit the same CTA then
+//    several), until no child matches.  Every row first checks, in parallel,
+//    whether it matches the target at its parent, so a level of the walk is
+//    one ballot.  In tsd_accept_commit the same CTA then
 //    commits the accepted path (the commit of tsd_commit_path, with the path
 //    taken from shared memory); its scratch-pad K/V rows were prefetched into
 //    L2 at the kernel's start, so the copy reads L2.
@@ -47,7 +48,6 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
   __shared__ uint64_t s_mask[kMaxR];
   __shared__ uint8_t s_leaf[kMaxR];
   __shared__ int32_t s_path[kCommitMaxRows];
-  __shared__ int32_t s_child[kMaxR];
   __shared__ int s_P, s_L;
   __shared__ CommitSmem s_commit;
   const int b = blockIdx.x;
@@ -68,7 +68,8 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
   // tree metadata, then tgt[r]: the largest of the row's chunk maxima.  Warp
   // w takes rows w, w+32, ...; its lanes split the (at most 256) chunks and
   // load them all at once.
-  for (int r = threadIdx.x; r < R; r += 32 * kWalkWarps) {
+  if (threadIdx.x < R) {   // (R <= 65: one row per thread)
+    const int r = threadIdx.x;
     s_tok[r] = token[o + r];
     s_par[r] = parent[o + r];
     s_mask[r] = mask[o + r];
@@ -94,31 +95,42 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
   }
   __syncthreads();
   if (warp == 0) {
-    bool bad = false;
-    for (int r = lane; r < R; r += 32) {
-      const int32_t p = s_par[r];
-      if (r > 0 && (p < 0 || p >= r)) bad = true;
-    }
-    bad = __any_sync(kFull, bad);
-    __syncwarp();
-
-    // the lowest matching child of every row u (parent[c] == u and token[c]
-    // == tgt[u]): each row c posts itself to its parent, so the walk below
-    // is one shared-memory read per level
-    for (int r = lane; r < R; r += 32) s_child[r] = R;
-    __syncwarp();
-    if (!bad)
-      for (int c = 1 + lane; c < R; c += 32) {
+    // (Short serial code: loops whose trip count differs between lanes cost
+    // far more than guarded straight-line chunks, so rows are taken in fixed
+    // chunks c = 1 + lane + 32 j, j < 2, covering rows 1..64.)
+    // Per row: its parent, whether the tree is valid there (0 <= parent < c),
+    // whether it matches the target at its parent (token[c] == tgt[parent]),
+    // and whether it is a leaf (for the chain id).
+    int pc[2];
+    bool mc[2], ok = true;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int c = 1 + lane + 32 * j;
+      pc[j] = -1;
+      mc[j] = false;
+      if (c < R) {
         const int p = s_par[c];
-        if (s_tok[c] == s_tgt[p]) atomicMin(&s_child[p], c);
+        const bool valid = p >= 0 && p < c;
+        ok = ok && valid;
+        pc[j] = p;
+        mc[j] = valid && s_tok[c] == s_tgt[valid ? p : 0];
       }
-    __syncwarp();
+    }
+    bool bad = !__all_sync(kFull, ok);
 
+    // the walk: a level is one ballot per 32 rows (the lowest matching child of u)
     int32_t* rows = accept_rows + (long)b * (S + 1);
     int u = 0, L = 0;
     if (!bad) {
       for (;;) {
-        const int found = s_child[u];
+        int found = R;
+        const unsigned b0 = __ballot_sync(kFull, mc[0] && pc[0] == u);
+        if (b0) {
+          found = __ffs(b0);
+        } else {
+          const unsigned b1 = __ballot_sync(kFull, mc[1] && pc[1] == u);
+          if (b1) found = 32 + __ffs(b1);
+        }
         if (found == R) break;
         if (L == S) { bad = true; break; }
         ++L;
@@ -134,18 +146,20 @@ accept_walk_kernel(const uint64_t* __restrict__ part, int R, int S, int nchunk,
       u = 0;
       L = 0;
     }
-    __syncwarp();
-    for (int i = lane; i <= S; i += 32)
-      if (i == 0) rows[0] = s_path[0] = 0;
-      else if (i > L) rows[i] = s_path[i] = -1;
+    if (lane <= S) {   // (S <= 16)
+      if (lane == 0) rows[0] = s_path[0] = 0;
+      else if (lane > L) rows[lane] = s_path[lane] = -1;
+    }
 
+    // chain id: the lowest leaf whose ancestor-or-self set holds u
     int chain = -1;
     if (L > 0) {
-      for (int base = 1; base < R && chain < 0; base += 32) {
-        const int c = base + lane;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = 1 + lane + 32 * j;
         const bool hit = c < R && s_leaf[c] && ((s_mask[c] >> (u - 1)) & 1ull);
         const unsigned bal = __ballot_sync(kFull, hit);
-        if (bal) chain = base + __ffs(bal) - 1;
+        if (chain < 0 && bal) chain = 32 * j + __ffs(bal);
       }
     }
     if (lane == 0) {

@@ -81,14 +81,16 @@ __device__ __forceinline__ void commit_request(const CommitArgs& a, CommitSmem& 
     const int per_row = a.Hkv * per_head;
     const int work = (L + 1) * per_row;
     const long hstride = a.page_size ? a.page_size : a.cap;
-    for (int w0 = tid; w0 < work; w0 += kThreads * kCommitUnroll) {
+    // (the same trip count for every thread: a loop whose count differs
+    // between the lanes of a warp costs far more than a guarded body)
+    for (int w0 = 0; w0 < work; w0 += kThreads * kCommitUnroll) {
       // all loads of the batch first, then the stores (the stores could alias
       // the sources as far as the compiler knows)
       int4 v[kCommitUnroll];
       int4* dst[kCommitUnroll];
 #pragma unroll
       for (int u = 0; u < kCommitUnroll; ++u) {
-        const int w = w0 + u * kThreads;
+        const int w = w0 + tid + u * kThreads;
         dst[u] = nullptr;
         if (w < work) {
           const int i = w / per_row;

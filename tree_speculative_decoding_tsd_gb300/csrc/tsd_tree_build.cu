@@ -261,11 +261,22 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   // Rows past the kept count (adaptive mode only) are inert padding: token -1
   // (no target token matches it), parent 0, depth 0, score 0, mask 0, not a
   // leaf, so verify, walk and commit treat them as never accepted.
-  for (int r = lane; r <= D; r += 32) s.has_child[r] = 0;
+  // (rows in fixed chunks r = lane + 32 j, j < 3, covering rows 0..64: a
+  // loop whose trip count differs between lanes costs far more)
+#pragma unroll
+  for (int j = 0; j < 3; ++j)
+    if (lane + 32 * j <= D) s.has_child[lane + 32 * j] = 0;
   __syncwarp();
-  for (int r = 1 + lane; r <= kept; r += 32) s.has_child[(s.r_dpr[r] >> 8) & 0xff] = 1;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int r = lane + 32 * j;
+    if (r >= 1 && r <= kept) s.has_child[(s.r_dpr[r] >> 8) & 0xff] = 1;
+  }
   __syncwarp();
-  for (int r = lane; r <= D; r += 32) {
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int r = lane + 32 * j;
+    if (r > D) continue;
     if (r <= kept) {
       const int32_t dpr = s.r_dpr[r];
       const int d = dpr & 0xff;
