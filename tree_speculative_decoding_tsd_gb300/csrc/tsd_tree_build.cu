@@ -104,9 +104,9 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
   // (where the popping warp would wait for it)
   const int32_t root = threadIdx.x == 0 ? root_tok[b] : 0;
   // adaptive mode: round cost of a tree with n nodes, fp32 C_d + C_v(n)
-  if (adaptive)
-    for (int n = threadIdx.x; n <= D; n += blockDim.x)
-      s.cost[n] = __fadd_rn(cost_d[b], cost_v[(long)b * R + n]);
+  // (zeros without a table: the pops read it in either mode)
+  for (int n = threadIdx.x; n <= D; n += blockDim.x)
+    s.cost[n] = adaptive ? __fadd_rn(cost_d[b], cost_v[(long)b * R + n]) : 0.f;
 
   // ---- warp p merges the chunk lists of position p into its top-k ----
   // (at most kScanMaxCand candidates: every lane loads its share up front)
@@ -168,19 +168,23 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
     const uint64_t pm = s.r_mask[par];
     const float h_sc = __shfl_sync(kFull, l_sc[0], 0);     // L[0]
     const int32_t h_dpr = __shfl_sync(kFull, l_dpr[0], 0);
-    if (adaptive) {
-      const float acc1 = __fadd_rn(acc, t_sc);
-      if (!(__fmul_rn(acc1, s.cost[row - 1]) > __fmul_rn(acc, s.cost[row]))) {
-        kept = row - 1;
-        break;
-      }
-      acc = acc1;
-    }
+    // (branch-free where it can be: a branch costs this serial loop more
+    // than the selects it saves)
+    // adaptive stop: the objective would fall with this node (the cost
+    // table is read in either mode; without one the test is masked off)
+    const float acc1 = __fadd_rn(acc, t_sc);
+    const bool stop =
+        adaptive && !(__fmul_rn(acc1, s.cost[row - 1]) > __fmul_rn(acc, s.cost[row]));
+    acc = acc1;
+    // (a stopped row is written too: rows past the kept count are never read)
     s.r_sc[row] = t_sc;
     s.r_dpr[row] = t_dpr;
     s.r_mask[row] = pm | (1ull << (row - 1));
     // nothing is popped after the last row: no new entries
-    if (row == D) break;
+    if (stop || row == D) {
+      kept = stop ? row - 1 : D;
+      break;
+    }
 
     // the candidates: next sibling (depth d, rank rk + 1), first child
     // (depth d + 1, rank 0); on equal scores the sibling, less deep, first
@@ -217,15 +221,9 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       }
     }
     // places in L' = L with the candidates merged in
-    int P1 = kNone, P2 = kNone;
-    if (sib && child) {
-      if (c1 >= c2) { P1 = p1; P2 = p2 + 1; }
-      else { P2 = p2; P1 = p1 + 1; }
-    } else if (sib) {
-      P1 = p1;
-    } else if (child) {
-      P2 = p2;
-    }
+    const bool c1_first = c1 >= c2;
+    const int P1 = sib ? p1 + (child && !c1_first ? 1 : 0) : kNone;
+    const int P2 = child ? p2 + (sib && c1_first ? 1 : 0) : kNone;
     // the next best entry is L'[0]; the new L[j] is L'[j + 1], a candidate
     // or L[j + 1 - (candidates placed before it)]
     float g_sc[kSlots];
@@ -241,18 +239,16 @@ best_first_tree_kernel(const uint64_t* __restrict__ part, int S, int k, int D, i
       for (int jj = 1; jj < kSlots; ++jj) {
         const float a = __shfl_sync(kFull, l_sc[jj], sl);
         const int32_t ad = __shfl_sync(kFull, l_dpr[jj], sl);
-        if (sj == jj) { vs = a; vd = ad; }
+        vs = sj == jj ? a : vs;
+        vd = sj == jj ? ad : vd;
       }
-      if (i == P1) { vs = c1; vd = c1_dpr; }
-      else if (i == P2) { vs = c2; vd = c2_dpr; }
-      g_sc[j] = vs;
-      g_dpr[j] = vd;
+      g_sc[j] = i == P1 ? c1 : (i == P2 ? c2 : vs);
+      g_dpr[j] = i == P1 ? c1_dpr : (i == P2 ? c2_dpr : vd);
     }
 #pragma unroll
     for (int j = 0; j < kSlots; ++j) { l_sc[j] = g_sc[j]; l_dpr[j] = g_dpr[j]; }
-    if (P1 == 0) { t_sc = c1; t_dpr = c1_dpr; }
-    else if (P2 == 0) { t_sc = c2; t_dpr = c2_dpr; }
-    else { t_sc = h_sc; t_dpr = h_dpr; }
+    t_sc = P1 == 0 ? c1 : (P2 == 0 ? c2 : h_sc);
+    t_dpr = P1 == 0 ? c1_dpr : (P2 == 0 ? c2_dpr : h_dpr);
     nl += (sib ? 1 : 0) + (child ? 1 : 0) - 1;
   }
   __syncwarp();
