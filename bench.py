@@ -315,6 +315,7 @@ CALL_SOURCES = {
                "tsd_verify.cuh", "tsd_tcgen05.cuh", "tsd_common.cuh"],
     "accept": ["tsd_accept.cu", "tsd_scan.cuh", "tsd_commit.cuh", "tsd_common.cuh"],
     "commit": ["tsd_commit.cu", "tsd_commit.cuh", "tsd_common.cuh"],
+    "accept_commit": ["tsd_accept.cu", "tsd_scan.cuh", "tsd_commit.cuh", "tsd_common.cuh"],
 }
 
 
