@@ -67,7 +67,7 @@ typedef struct CUstream_st* tsd_stream_t;
 typedef enum {
   TSD_OK = 0,
   TSD_ERR_INVALID_ARG = 1,    /* bad size, null or misaligned pointer, short workspace */
-  TSD_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+  TSD_ERR_UNSUPPORTED = 2,    /* a valid request the library does not implement */
   TSD_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
   TSD_ERR_DEVICE = 4,         /* reserved: device-side problems go to the err word */
   TSD_ERR_DEVICE_TIMEOUT = 5  /* a bounded device wait gave up */
