@@ -361,6 +361,70 @@ def test_accept_walk_page_fixtures(fixture):
     assert got["bonus"][0] == g["bonus"][0] and got["chain_id"][0] == g["chain_id"][0]
 
 
+def _deep_row_tree():
+    """A 65-row tree whose accepted path runs through rows 40, 60, 61, 64 (all
+    past the first 32 child rows) with two children of row 60 carrying the
+    same token (the lower row must win) and the chain leaf in the same rows."""
+    R, S, V = 65, 4, 2048
+    parent = np.zeros(R, np.int32)
+    parent[0] = -1
+    parent[45:61] = 40
+    parent[61:64] = 60
+    parent[64] = 61
+    token = (1000 + np.arange(R)).astype(np.int32)
+    token[0] = 7
+    token[61] = token[62] = 777
+    depth = np.zeros(R, np.int32)
+    mask = np.zeros(R, np.uint64)
+    for c in range(1, R):
+        depth[c] = depth[parent[c]] + 1
+        mask[c] = (mask[parent[c]] if parent[c] > 0 else np.uint64(0)) | np.uint64(1 << (c - 1))
+    has_child = np.zeros(R, bool)
+    has_child[parent[1:]] = True
+    tree = dict(token=token[None], parent=parent[None], depth=depth[None],
+                score=np.linspace(1.0, 0.01, R, dtype=np.float32)[None], mask=mask[None],
+                is_leaf=(~has_child).astype(np.uint8)[None])
+    tgt = np.full(R, 5, np.int64)
+    tgt[0], tgt[40], tgt[60], tgt[61] = token[40], token[60], 777, token[64]
+    tl = torch.full((1, R, V), -1.0)
+    for r in range(R):
+        tl[0, r, tgt[r]] = 1.0
+    return tree, tl, R, S, V
+
+
+def test_accept_walk_rows_past_the_first_warp():
+    """Rows 33-64 (the second chunk of the walk's row-per-lane layout): the
+    accepted path, the lowest of two matching siblings, and the chain leaf
+    all lie there; the separate walk and the fused walk + commit agree with
+    the oracle."""
+    tree, tl, R, S, V = _deep_row_tree()
+    tgt = oracle.argmax(tl.numpy())
+    ref = oracle.accept_walk(tgt, tree, S)
+    assert list(ref["accept_rows"][0]) == [0, 40, 60, 61, 64] and ref["chain_id"][0] == 64
+    step = TreeVerifyStep(1, S, V, 8, R - 1, 1, 1, 64, 64, 16, torch.float32, False, 0.125, DEV)
+    set_tree(step, tree)
+    assert_walk_equal(run_walk(step, tl), ref, tgt)
+    # fused: also the commit of rows 0, 40, 60, 61, 64 at positions P..P+4
+    g = torch.Generator().manual_seed(11)
+    kt = torch.randn((1, R, 1, 64), generator=g)
+    vt = torch.randn((1, R, 1, 64), generator=g)
+    kc = torch.zeros((1, 1, 16, 64))
+    vc = torch.zeros((1, 1, 16, 64))
+    plen = torch.tensor([3], dtype=torch.int32)
+    kc_ref, vc_ref, pl_ref = W.bits(kc).copy(), W.bits(vc).copy(), plen.numpy().copy()
+    oracle.commit(W.bits(kt), W.bits(vt), ref["accept_rows"], ref["accept_len"], kc_ref, vc_ref,
+                  pl_ref, S)
+    step.walk.accept_len.zero_()
+    gtl, gkt, gvt, gkc, gvc, gpl = gpu(tl, kt, vt, kc, vc, plen)
+    step.accept_commit(gtl, gkt, gvt, gkc, gvc, gpl)
+    torch.cuda.synchronize()
+    for key in ("accept_len", "accept_rows", "bonus", "chain_id"):
+        np.testing.assert_array_equal(getattr(step.walk, key).cpu().numpy(), ref[key])
+    np.testing.assert_array_equal(W.bits(gkc.cpu()), kc_ref)
+    np.testing.assert_array_equal(W.bits(gvc.cpu()), vc_ref)
+    assert int(gpl[0]) == 3 + 1 + 4 and int(step.err[0]) == 0
+
+
 def test_accept_walk_reports_malformed_tree():
     d = inputs("toy")
     w, tree = d["w"], dict(d["tree"])
