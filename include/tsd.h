@@ -11,7 +11,8 @@
  *   tsd_accept_walk       target argmax per node, greedy walk to the accepted
  *                         path, bonus (correction) token, chain id
  *   tsd_commit_path       copy the accepted path's scratch KV into the cache
- *   tsd_accept_commit     the walk and the commit in one call
+ *   tsd_accept_commit     the walk and the commit in one call (also in two
+ *                         parts: tsd_target_argmax, tsd_walk_commit)
  *
  * Sources of the operations (web pages, by title and section):
  *   "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4 for
@@ -399,6 +400,37 @@ tsd_status tsd_accept_commit(const float* logits, int B, int D, int S, int V,
                              int page_size, int num_pages, int32_t* prefix_len,
                              void* ws, size_t ws_bytes, int32_t* err,
                              tsd_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * tsd_target_argmax, tsd_walk_commit
+ *
+ * tsd_accept_commit in two parts.  The target argmax reads only the logits,
+ * so a caller may run it on another stream, concurrently with the tree build
+ * and the attention of the same step, and join the streams before the walk.
+ *   tsd_target_argmax  writes the per-chunk argmax candidates of every row
+ *                      of logits [B][1+D][V] to ws
+ *                      (tsd_accept_walk_workspace_size(B, D, V) bytes).
+ *   tsd_walk_commit    reads them from the same ws, merges them into tgt
+ *                      and does the rest of tsd_accept_commit (walk, bonus,
+ *                      chain id, commit); V is the logits' row length.
+ * The caller orders the two (the argmax must have completed, with its writes
+ * visible, before the walk starts: same stream, or an event between the
+ * streams) and gives each its own ws while calls overlap.  In order on one
+ * stream they are exactly tsd_accept_commit; arguments and device-side
+ * errors as there.
+ * -------------------------------------------------------------------------- */
+tsd_status tsd_target_argmax(const float* logits, int B, int D, int V, void* ws,
+                             size_t ws_bytes, tsd_stream_t stream);
+
+tsd_status tsd_walk_commit(int B, int D, int S, int V, const int32_t* token,
+                           const int32_t* parent, const uint64_t* mask,
+                           const uint8_t* is_leaf, int32_t* tgt, int32_t* accept_len,
+                           int32_t* accept_rows, int32_t* bonus, int32_t* chain_id,
+                           const tsd_attn_desc* desc, const void* ktree,
+                           const void* vtree, void* kcache, void* vcache,
+                           const int32_t* page_table, int max_pages, int page_size,
+                           int num_pages, int32_t* prefix_len, const void* ws,
+                           size_t ws_bytes, int32_t* err, tsd_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * tsd_commit_path

@@ -143,6 +143,30 @@ def test_accept_commit_rejects(args):
     assert st == T.TSD_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("args", [dict(B=0), dict(D=65), dict(V=0), dict(logits=N), dict(logits=U),
+                                  dict(ws=N), dict(ws_bytes=0)])
+def test_target_argmax_rejects(args):
+    kw = dict(B=2, D=4, V=32, logits=A, ws=A, ws_bytes=1 << 20)
+    kw.update(args)
+    st = T.lib.tsd_target_argmax(kw["logits"], kw["B"], kw["D"], kw["V"], kw["ws"], kw["ws_bytes"],
+                                 N)
+    assert st == T.TSD_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", [dict(), dict(B=3), dict(S=17), dict(V=0), dict(tok=N),
+                                  dict(kt=N), dict(ws_bytes=0), dict(page_size=-1)])
+def test_walk_commit_rejects(args):
+    kw = dict(B=2, D=4, S=3, V=32, tok=A, kt=A, ws_bytes=1 << 20, page_size=0)
+    kw.update(args)
+    d = _desc(cap=64)
+    if not args:
+        d.R = 9     # desc R != D + 1
+    st = T.lib.tsd_walk_commit(kw["B"], kw["D"], kw["S"], kw["V"], kw["tok"], A, A, A, N, A, A, A,
+                               A, ctypes.byref(d), kw["kt"], A, A, A, N, 0, kw["page_size"], 0, A,
+                               A, kw["ws_bytes"], N, N)
+    assert st == T.TSD_ERR_INVALID_ARG
+
+
 def test_workspace_sizes_are_deterministic_and_scale():
     a = T.tsd_tree_build_workspace_size(32, 7, 151936, 8)
     assert a == T.tsd_tree_build_workspace_size(32, 7, 151936, 8) and a > 0

@@ -851,7 +851,7 @@ def _oracle_round(w, d, tree, q, kc, vc, plen, kt, vt, tl, sel):
     return ref_out, tgt, walk, kc_ref, vc_ref, pl_ref
 
 
-@pytest.mark.parametrize("case", ["batched", "batched_adaptive", "qwen"])
+@pytest.mark.parametrize("case", ["batched", "batched_adaptive", "batched_overlap", "qwen"])
 def test_captured_round_matches_oracle(case):
     """The whole round recorded as one CUDA graph (TreeVerifyStep.capture, the
     flow the benchmark times) matches the oracle replay after replay -- tree,
@@ -879,12 +879,15 @@ def test_captured_round_matches_oracle(case):
         return gpu(d["probs"], d["root"], q, kc.clone(), None if vc is None else vc.clone(),
                    plen.clone(), kt, vt, tl)
 
-    eager = TreeVerifyStep.for_workload(w, DEV)
+    # "batched_overlap": the target argmax on the second stream (forked and
+    # joined inside the graph)
+    ov = True if case.endswith("overlap") else None
+    eager = TreeVerifyStep.for_workload(w, DEV, overlap_argmax=ov)
     ge = fresh()
     eager._round(*ge, *extra, None)
     torch.cuda.synchronize()
 
-    graphed = TreeVerifyStep.for_workload(w, DEV)
+    graphed = TreeVerifyStep.for_workload(w, DEV, overlap_argmax=ov)
     gg = fresh()
     g = graphed.capture(*gg, *extra)
     for _ in range(2):
@@ -1190,6 +1193,45 @@ def test_accept_commit_matches_oracle_walk_and_commit(name, over, paged):
         assert err & T.TSD_DEV_ERR_MASK == T.TSD_DEV_ERR_CAPACITY and err & 0xFFFFFF == over_b[-1]
     else:
         assert err == 0
+
+
+@pytest.mark.parametrize("name,over", [("qwen", {}), ("batched", dict(B=6, V=20000))])
+def test_argmax_then_walk_commit_equals_the_fused_call(name, over):
+    """tsd_target_argmax then tsd_walk_commit on one stream, and with the
+    argmax on a second stream joined by an event, against tsd_accept_commit:
+    identical outputs, cache and prefix lengths."""
+    d = inputs(name, **over)
+    w, tree = d["w"], d["tree"]
+    q, kc, vc, plen, kt, vt = attn_inputs(w)
+    tl = W.target_logits(w, torch.from_numpy(tree["depth"]), d["logits"])
+    results = []
+    for mode in ("fused", "split", "two streams"):
+        step = TreeVerifyStep.for_workload(w, DEV)
+        set_tree(step, tree)
+        gtl, gkt, gvt, gkc, gvc, gpl = gpu(tl, kt, vt, kc, vc, plen)
+        t, wk = step.tree, step.walk
+        main = torch.cuda.current_stream()
+        if mode == "fused":
+            step.accept_commit(gtl, gkt, gvt, gkc, gvc, gpl)
+        else:
+            side = step.side if mode == "two streams" else main
+            if side is not main:
+                step.ev_fork.record(main)
+                side.wait_event(step.ev_fork)
+            T.tsd_target_argmax(gtl, step.ws_walk, side)
+            if side is not main:
+                step.ev_join.record(side)
+                main.wait_event(step.ev_join)
+            T.tsd_walk_commit(w.V, w.S, t.token, t.parent, t.mask, t.is_leaf, wk.tgt, wk.accept_len,
+                              wk.accept_rows, wk.bonus, wk.chain_id, step.desc, gkt, gvt, gkc, gvc,
+                              gpl, step.ws_walk, step.err, main)
+        torch.cuda.synchronize()
+        results.append([x.cpu() for x in (wk.tgt, wk.accept_len, wk.accept_rows, wk.bonus,
+                                          wk.chain_id, gkc, gpl, step.err)]
+                       + ([] if gvc is None else [gvc.cpu()]))
+    for other in results[1:]:
+        for a, b in zip(results[0], other):
+            assert torch.equal(a, b)
 
 
 def test_paged_bad_page_is_reported_not_read():

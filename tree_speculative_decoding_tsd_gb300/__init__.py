@@ -54,8 +54,8 @@ EXPORTED = ("tsd_status_string", "tsd_version", "tsd_tree_build_workspace_size",
             "tsd_verify_workspace_size",
             "tsd_tree_verify_attn", "tsd_tree_verify_attn_paged", "tsd_commit_path_paged",
             "tsd_accept_walk_workspace_size", "tsd_accept_walk", "tsd_accept_walk_static",
-            "tsd_commit_path", "tsd_accept_commit", "tsd_set_verify_path",
-            "tsd_set_wait_budget")
+            "tsd_commit_path", "tsd_accept_commit", "tsd_target_argmax", "tsd_walk_commit",
+            "tsd_set_verify_path", "tsd_set_wait_budget")
 
 
 class TsdError(RuntimeError):
@@ -111,6 +111,12 @@ def _load():
                                       ctypes.POINTER(tsd_attn_desc), P, P, P, P, P, I, I, I, P,
                                       P, Z, P, P]
     lib.tsd_accept_commit.restype = I
+    lib.tsd_target_argmax.argtypes = [P, I, I, I, P, Z, P]
+    lib.tsd_target_argmax.restype = I
+    lib.tsd_walk_commit.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P,
+                                    ctypes.POINTER(tsd_attn_desc), P, P, P, P, P, I, I, I, P, P,
+                                    Z, P, P]
+    lib.tsd_walk_commit.restype = I
     lib.tsd_set_verify_path.argtypes = [I]
     lib.tsd_set_verify_path.restype = I
     lib.tsd_set_wait_budget.argtypes = [ctypes.c_longlong]
@@ -406,6 +412,44 @@ def tsd_commit_path(desc, S, ktree, vtree, accept_rows, accept_len, kcache, vcac
         ctypes.byref(d), S, pkt, pvt, par, pal, pkc, pvc, ppl, _err(err), _stream(stream)))
 
 
+def _commit_targets(d, kcache, vcache, page_table, page_size):
+    dt = _attn_dtype(d)
+    if page_table is None:
+        pkc = _t(kcache, "kcache", dt, (d.B, d.Hkv, d.cap, d.dk))
+        pvc = None if d.v_aliases_k else _t(vcache, "vcache", dt, (d.B, d.Hkv, d.cap, d.dv))
+        return pkc, pvc, (None, 0, 0, 0)
+    npg, mp = kcache.shape[0], page_table.shape[1]
+    pkc = _t(kcache, "kpool", dt, (npg, d.Hkv, page_size, d.dk))
+    pvc = None if d.v_aliases_k else _t(vcache, "vpool", dt, (npg, d.Hkv, page_size, d.dv))
+    return pkc, pvc, (_t(page_table, "page_table", _I32, (d.B, mp)), mp, page_size, npg)
+
+
+def tsd_target_argmax(logits, ws, stream=None):
+    """The argmax part of tsd_accept_commit: per-chunk candidates of every row into ws."""
+    B, R, V = logits.shape
+    _check("tsd_target_argmax", _L().tsd_target_argmax(
+        _t(logits, "logits", _F32), B, R - 1, V, _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def tsd_walk_commit(V, S, token, parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus,
+                    chain_id, desc, ktree, vtree, kcache, vcache, prefix_len, ws, err=None,
+                    stream=None, page_table=None, page_size=0):
+    """The rest of tsd_accept_commit, from the candidates tsd_target_argmax left in ws."""
+    d = desc
+    B, R = token.shape
+    if B != d.B or R != d.R:
+        raise ValueError("tsd_walk_commit: tree batch / rows do not match desc (B, R)")
+    pkt, pvt, _, _, ppl = _commit_common(d, S, ktree, vtree, accept_rows, accept_len, prefix_len)
+    pkc, pvc, paging = _commit_targets(d, kcache, vcache, page_table, page_size)
+    _check("tsd_walk_commit", _L().tsd_walk_commit(
+        B, R - 1, S, V, _t(token, "token", _I32, (B, R)), _t(parent, "parent", _I32, (B, R)),
+        _t(mask, "mask", _MASK, (B, R)), _t(is_leaf, "is_leaf", _U8, (B, R)),
+        _t(tgt, "tgt", _I32, (B, R)), _t(accept_len, "accept_len", _I32, (B,)),
+        _t(accept_rows, "accept_rows", _I32, (B, S + 1)), _t(bonus, "bonus", _I32, (B,)),
+        _t(chain_id, "chain_id", _I32, (B,)), ctypes.byref(d), pkt, pvt, pkc, pvc, *paging, ppl,
+        _ptr(ws), _nbytes(ws), _err(err), _stream(stream)))
+
+
 def tsd_accept_commit(logits, S, token, parent, mask, is_leaf, tgt, accept_len, accept_rows,
                       bonus, chain_id, desc, ktree, vtree, kcache, vcache, prefix_len, ws,
                       err=None, stream=None, page_table=None, page_size=0):
@@ -415,21 +459,12 @@ def tsd_accept_commit(logits, S, token, parent, mask, is_leaf, tgt, accept_len, 
     the page pools [num_pages][Hkv][page_size][d] of tsd_commit_path_paged.
     """
     d = desc
-    dt = _attn_dtype(d)
     walk = _walk_args(logits, S, token, parent, mask, is_leaf, tgt, accept_len, accept_rows,
                       bonus, chain_id)
     if walk[1] != d.B or walk[2] + 1 != d.R:
         raise ValueError("tsd_accept_commit: logits batch / rows do not match desc (B, R)")
     pkt, pvt, _, _, ppl = _commit_common(d, S, ktree, vtree, accept_rows, accept_len, prefix_len)
-    if page_table is None:
-        pkc = _t(kcache, "kcache", dt, (d.B, d.Hkv, d.cap, d.dk))
-        pvc = None if d.v_aliases_k else _t(vcache, "vcache", dt, (d.B, d.Hkv, d.cap, d.dv))
-        paging = (None, 0, 0, 0)
-    else:
-        npg, mp = kcache.shape[0], page_table.shape[1]
-        pkc = _t(kcache, "kpool", dt, (npg, d.Hkv, page_size, d.dk))
-        pvc = None if d.v_aliases_k else _t(vcache, "vpool", dt, (npg, d.Hkv, page_size, d.dv))
-        paging = (_t(page_table, "page_table", _I32, (d.B, mp)), mp, page_size, npg)
+    pkc, pvc, paging = _commit_targets(d, kcache, vcache, page_table, page_size)
     _check("tsd_accept_commit", _L().tsd_accept_commit(
         *walk, ctypes.byref(d), pkt, pvt, pkc, pvc, *paging, ppl, _ptr(ws), _nbytes(ws),
         _err(err), _stream(stream)))

@@ -217,6 +217,71 @@ extern "C" tsd_status tsd_accept_walk(const float* logits, int B, int D, int S, 
   return cuda_status();
 }
 
+namespace {
+
+tsd_status walk_tree_args(int B, int D, int S, int V, const int32_t* token, const int32_t* parent,
+                          const uint64_t* mask, const uint8_t* is_leaf, const int32_t* tgt,
+                          const int32_t* accept_len, const int32_t* accept_rows,
+                          const int32_t* bonus, const int32_t* chain_id, const int32_t* err) {
+  if (B < 1 || D < 1 || D > kMaxR - 1 || S < 1 || S > 16 || V < 1 || V > (1 << 30))
+    return TSD_ERR_INVALID_ARG;
+  if ((long)B * (D + 1) > (1l << 24)) return TSD_ERR_INVALID_ARG;
+  if (!ok_ptr(token) || !ok_ptr(parent) || !ok_ptr(mask) || !ok_ptr(is_leaf) ||
+      !ok_opt_ptr(tgt) || !ok_ptr(accept_len) || !ok_ptr(accept_rows) || !ok_ptr(bonus) ||
+      !ok_ptr(chain_id) || !ok_opt_ptr(err))
+    return TSD_ERR_INVALID_ARG;
+  return TSD_OK;
+}
+
+// The argmax part of the walk: per-chunk argmax candidates of every tree
+// row's target logits into ws.
+void launch_target_argmax(const float* logits, int B, int D, int V, void* ws, cudaStream_t st) {
+  const long rows = (long)B * (D + 1);
+  const ScanGeom g = scan_geometry(rows, V, 1, true);
+  launch(vocab_scan_kernel<true>, dim3((unsigned)(rows * g.nchunk)), dim3(kScanThreads), 0, st,
+      logits, V, 1, g.nchunk, g.chunk_len, (uint64_t*)ws, g.one_wave, nullptr, 1);
+}
+
+}  // namespace
+
+extern "C" tsd_status tsd_target_argmax(const float* logits, int B, int D, int V, void* ws,
+                                        size_t ws_bytes, tsd_stream_t stream) {
+  if (B < 1 || D < 1 || D > kMaxR - 1 || V < 1 || V > (1 << 30)) return TSD_ERR_INVALID_ARG;
+  if ((long)B * (D + 1) > (1l << 24)) return TSD_ERR_INVALID_ARG;
+  if (!ok_ptr(logits)) return TSD_ERR_INVALID_ARG;
+  if (ws_bytes < tsd_accept_walk_workspace_size(B, D, V) || !ok_ptr(ws)) return TSD_ERR_INVALID_ARG;
+  launch_target_argmax(logits, B, D, V, ws, (cudaStream_t)stream);
+  return cuda_status();
+}
+
+extern "C" tsd_status tsd_walk_commit(int B, int D, int S, int V, const int32_t* token,
+                                      const int32_t* parent, const uint64_t* mask,
+                                      const uint8_t* is_leaf, int32_t* tgt, int32_t* accept_len,
+                                      int32_t* accept_rows, int32_t* bonus, int32_t* chain_id,
+                                      const tsd_attn_desc* desc, const void* ktree,
+                                      const void* vtree, void* kcache, void* vcache,
+                                      const int32_t* page_table, int max_pages, int page_size,
+                                      int num_pages, int32_t* prefix_len, const void* ws,
+                                      size_t ws_bytes, int32_t* err, tsd_stream_t stream) {
+  const tsd_status wst = walk_tree_args(B, D, S, V, token, parent, mask, is_leaf, tgt,
+                                        accept_len, accept_rows, bonus, chain_id, err);
+  if (wst != TSD_OK) return wst;
+  if (desc == nullptr || desc->B != B || desc->R != D + 1 || page_size < 0)
+    return TSD_ERR_INVALID_ARG;
+  CommitArgs ca;
+  const tsd_status cst = commit_args(desc, S, ktree, vtree, accept_rows, accept_len, kcache,
+                                     vcache, page_table, max_pages, page_size, num_pages,
+                                     prefix_len, err, &ca);
+  if (cst != TSD_OK) return cst;
+  if (ws_bytes < tsd_accept_walk_workspace_size(B, D, V) || !ok_ptr(ws)) return TSD_ERR_INVALID_ARG;
+  const int R = D + 1;
+  const ScanGeom g = scan_geometry((long)B * R, V, 1, true);
+  launch(accept_walk_kernel<true>, dim3(B), dim3(32 * kWalkWarps), 0, (cudaStream_t)stream,
+      (const uint64_t*)ws, R, S, g.nchunk, token, parent, mask, is_leaf, tgt, accept_len,
+      accept_rows, bonus, chain_id, err, ca);
+  return cuda_status();
+}
+
 extern "C" tsd_status tsd_accept_commit(const float* logits, int B, int D, int S, int V,
                                         const int32_t* token, const int32_t* parent,
                                         const uint64_t* mask, const uint8_t* is_leaf,
@@ -227,13 +292,11 @@ extern "C" tsd_status tsd_accept_commit(const float* logits, int B, int D, int S
                                         const int32_t* page_table, int max_pages, int page_size,
                                         int num_pages, int32_t* prefix_len, void* ws,
                                         size_t ws_bytes, int32_t* err, tsd_stream_t stream) {
-  if (B < 1 || D < 1 || D > kMaxR - 1 || S < 1 || S > 16 || V < 1 || V > (1 << 30))
-    return TSD_ERR_INVALID_ARG;
-  if ((long)B * (D + 1) > (1l << 24)) return TSD_ERR_INVALID_ARG;
-  if (!ok_ptr(logits) || !ok_ptr(token) || !ok_ptr(parent) || !ok_ptr(mask) ||
-      !ok_ptr(is_leaf) || !ok_opt_ptr(tgt) || !ok_ptr(accept_len) || !ok_ptr(accept_rows) ||
-      !ok_ptr(bonus) || !ok_ptr(chain_id) || !ok_opt_ptr(err))
-    return TSD_ERR_INVALID_ARG;
+  // both parts' checks before anything is enqueued
+  const tsd_status wst = walk_tree_args(B, D, S, V, token, parent, mask, is_leaf, tgt,
+                                        accept_len, accept_rows, bonus, chain_id, err);
+  if (wst != TSD_OK) return wst;
+  if (!ok_ptr(logits)) return TSD_ERR_INVALID_ARG;
   if (desc == nullptr || desc->B != B || desc->R != D + 1 || page_size < 0)
     return TSD_ERR_INVALID_ARG;
   CommitArgs ca;
@@ -241,19 +304,11 @@ extern "C" tsd_status tsd_accept_commit(const float* logits, int B, int D, int S
                                      vcache, page_table, max_pages, page_size, num_pages,
                                      prefix_len, err, &ca);
   if (cst != TSD_OK) return cst;
-  const size_t need = tsd_accept_walk_workspace_size(B, D, V);
-  if (ws_bytes < need || !ok_ptr(ws)) return TSD_ERR_INVALID_ARG;
-
-  const cudaStream_t st = (cudaStream_t)stream;
-  const int R = D + 1;
-  const long rows = (long)B * R;
-  const ScanGeom g = scan_geometry(rows, V, 1, true);
-  uint64_t* part = (uint64_t*)ws;
-  launch(vocab_scan_kernel<true>, dim3((unsigned)(rows * g.nchunk)), dim3(kScanThreads), 0, st,
-      logits, V, 1, g.nchunk, g.chunk_len, part, g.one_wave, nullptr, 1);
-  launch(accept_walk_kernel<true>, dim3(B), dim3(32 * kWalkWarps), 0, st, part, R, S, g.nchunk,
-      token, parent, mask, is_leaf, tgt, accept_len, accept_rows, bonus, chain_id, err, ca);
-  return cuda_status();
+  if (ws_bytes < tsd_accept_walk_workspace_size(B, D, V) || !ok_ptr(ws)) return TSD_ERR_INVALID_ARG;
+  launch_target_argmax(logits, B, D, V, ws, (cudaStream_t)stream);
+  return tsd_walk_commit(B, D, S, V, token, parent, mask, is_leaf, tgt, accept_len, accept_rows,
+                         bonus, chain_id, desc, ktree, vtree, kcache, vcache, page_table,
+                         max_pages, page_size, num_pages, prefix_len, ws, ws_bytes, err, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -13,7 +13,7 @@ import dataclasses
 import torch
 
 from . import (make_desc, tsd_accept_commit, tsd_accept_walk, tsd_accept_walk_workspace_size,
-               tsd_commit_path,
+               tsd_commit_path, tsd_target_argmax, tsd_walk_commit,
                tsd_tree_build, tsd_tree_build_adaptive, tsd_tree_build_conditioned,
                tsd_tree_build_workspace_size, tsd_tree_verify_attn, tsd_verify_workspace_size,
                workspace)
@@ -40,7 +40,7 @@ class WalkBuffers:
 
 class TreeVerifyStep:
     def __init__(self, B, S, V, k, D, Hq, Hkv, dk, dv, cap, dtype, v_aliases_k, scale,
-                 device="cuda"):
+                 device="cuda", overlap_argmax=None):
         self.B, self.S, self.V, self.k, self.D = B, S, V, k, D
         self.R = R = D + 1
         self.Hq, self.Hkv, self.dk, self.dv, self.cap = Hq, Hkv, dk, dv, cap
@@ -66,6 +66,24 @@ class TreeVerifyStep:
         self.ws_build = workspace(tsd_tree_build_workspace_size(B, S, V, k), dev)
         self.ws_verify = workspace(tsd_verify_workspace_size(self.desc), dev)
         self.ws_walk = workspace(tsd_accept_walk_workspace_size(B, D, V), dev)
+        # The target argmax of a round reads only the logits, so it may run on
+        # a second stream beside the tree build and the attention, the walk
+        # waiting for it (fork and join by events, also inside a captured
+        # graph).  Measured on a GB300 that pays when the logits are about as
+        # large as the attention's KV and large in absolute terms (32 requests
+        # of 1-4k prefixes: step 241 -> 231 us); where the attention dominates
+        # (32k prefixes) the argmax only competes with it (+6 us), and a small
+        # step loses its launch overlap to the fork and join (+4.6 us).  None
+        # chooses by those sizes.
+        es = 2 if dtype == torch.bfloat16 else 4
+        logits_bytes = B * R * V * 4
+        kv_bytes = B * Hkv * cap * (dk + (0 if v_aliases_k else dv)) * es
+        if overlap_argmax is None:
+            overlap_argmax = logits_bytes >= (64 << 20) and logits_bytes >= kv_bytes
+        self.overlap_argmax = bool(overlap_argmax)
+        self.side = torch.cuda.Stream(device=dev)
+        self.ev_fork = torch.cuda.Event()
+        self.ev_join = torch.cuda.Event()
 
     # the four calls -------------------------------------------------------
     def build(self, probs, root_tok, stream=None):
@@ -112,7 +130,9 @@ class TreeVerifyStep:
 
     def run(self, probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits,
             stream=None):
-        """The whole step: build -> verify -> accept + commit (asynchronous)."""
+        """The whole step: build -> verify -> target argmax, walk and commit
+        (asynchronous); with ``overlap_argmax`` the target argmax runs beside
+        build and verify on a second stream."""
         self._round(probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits, None,
                     None, stream)
 
@@ -146,14 +166,27 @@ class TreeVerifyStep:
 
     def _round(self, probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits,
                cost_d, cost_v, stream):
+        main = stream if stream is not None else torch.cuda.current_stream(probs.device)
+        if self.overlap_argmax:
+            self.ev_fork.record(main)
+            self.side.wait_event(self.ev_fork)
+            tsd_target_argmax(logits, self.ws_walk, self.side)
+            self.ev_join.record(self.side)
         if cost_v is None:
-            self.build(probs, root_tok, stream)
+            self.build(probs, root_tok, main)
         else:
-            self.build_adaptive(probs, root_tok, cost_d, cost_v, stream)
-        self.verify(q, kcache, vcache, prefix_len, ktree, vtree, stream)
-        self.accept_commit(logits, ktree, vtree, kcache, vcache, prefix_len, stream)
+            self.build_adaptive(probs, root_tok, cost_d, cost_v, main)
+        self.verify(q, kcache, vcache, prefix_len, ktree, vtree, main)
+        if not self.overlap_argmax:
+            self.accept_commit(logits, ktree, vtree, kcache, vcache, prefix_len, main)
+            return
+        main.wait_event(self.ev_join)
+        t, w = self.tree, self.walk
+        tsd_walk_commit(self.V, self.S, t.token, t.parent, t.mask, t.is_leaf, w.tgt,
+                        w.accept_len, w.accept_rows, w.bonus, w.chain_id, self.desc, ktree, vtree,
+                        kcache, vcache, prefix_len, self.ws_walk, self.err, main)
 
     @classmethod
-    def for_workload(cls, w, device="cuda"):
+    def for_workload(cls, w, device="cuda", overlap_argmax=None):
         return cls(w.B, w.S, w.V, w.k, w.D, w.Hq, w.Hkv, w.dk, w.dv, w.cap, w.torch_dtype,
-                   w.v_aliases_k, w.scale, device)
+                   w.v_aliases_k, w.scale, device, overlap_argmax)
