@@ -161,8 +161,8 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
   // only where the request is known before the prefix lengths are read.
   if (!lpt) {
     const int w = threadIdx.x >> 5, ln = threadIdx.x & 31;
-    const int hk0 = blockIdx.y / a.nrg, b0 = blockIdx.z;
-    const int kp0 = blockIdx.x * a.split_len;
+    const int hk0 = blockIdx.x / a.nrg, b0 = blockIdx.z;
+    const int kp0 = blockIdx.y * a.split_len;
     if (!kPaged && w < 4 && ln == 0) {
       const int t = w >> 1;
       const CUtensorMap* m = (w & 1) ? &maps.v : &maps.k;
@@ -171,7 +171,7 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
     } else if (w == 4) {
       // packed rows [p0, p1) of this row group: for each tree row, the heads
       // of this KV head are one contiguous run of q
-      const int p0 = (blockIdx.y % a.nrg) * rows_per_cta;
+      const int p0 = (blockIdx.x % a.nrg) * rows_per_cta;
       const int p1 = min(p0 + rows_per_cta, a.M);
       for (int tr = p0 / a.g + ln; tr <= (p1 - 1) / a.g; tr += 32) {
         const int h0 = max(p0, tr * a.g) - tr * a.g, h1 = min(p1, (tr + 1) * a.g) - tr * a.g;
@@ -201,8 +201,8 @@ verify_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Ve
   auto bar = [&](int i) { return bar0 + 8u * i; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int sp = blockIdx.x;
-  const int hk = blockIdx.y / a.nrg, rg = blockIdx.y % a.nrg;
+  const int sp = blockIdx.y;
+  const int hk = blockIdx.x / a.nrg, rg = blockIdx.x % a.nrg;
   int b = blockIdx.z;
   if (lpt) {
     // warp 0 ranks the requests (lane l holds requests l and l + 32); the one
@@ -759,7 +759,11 @@ void launch_tc(const TcMaps& maps, const VerifyArgs& a, const VerifyPlan& p, cud
   const uint32_t smem = TcLayout<N>::total + 1024;
   const auto kern = a.page_size > 0 ? verify_tc_kernel<N, true> : verify_tc_kernel<N, false>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  const dim3 grid(p.nsplit, a.Hkv * p.nrg, a.B);
+  // (KV head and row group fastest, then the split: the last CTAs of the
+  // grid are the last split, which only requests with the longest prefixes
+  // use, so a grid just past one wave ends with CTAs that return at once;
+  // the row groups of a head run side by side and share its tiles in L2)
+  const dim3 grid(a.Hkv * p.nrg, p.nsplit, a.B);
   launch(kern, dim3(grid), dim3(kThreadsTC), smem, st, maps, a, p.rb);
 }
 
