@@ -459,7 +459,7 @@ def run_ours(args, dist, config=None, lite=False):
         "data": "synthetic (seeded, shapes and distributions of the workload)",
         "config": {"workload": workload_desc(w), "nodes_per_step": nodes,
                    "launch": "cuda_graph" if graph is not None else "eager",
-                   "streams": ("2 (target argmax beside build and verify)"
+                   "streams": ("2 (target argmax beside the attention)"
                                if step.overlap_argmax else "1"),
                    "l2": "flushed before every timed step (memset of 2x L2, outside the events)",
                    "parallelism": f"replicas x{dist.world} (independent requests)"},

@@ -851,7 +851,7 @@ def _oracle_round(w, d, tree, q, kc, vc, plen, kt, vt, tl, sel):
     return ref_out, tgt, walk, kc_ref, vc_ref, pl_ref
 
 
-@pytest.mark.parametrize("case", ["batched", "batched_adaptive", "batched_overlap", "qwen"])
+@pytest.mark.parametrize("case", ["batched", "batched_adaptive", "batched_one_stream", "qwen"])
 def test_captured_round_matches_oracle(case):
     """The whole round recorded as one CUDA graph (TreeVerifyStep.capture, the
     flow the benchmark times) matches the oracle replay after replay -- tree,
@@ -879,9 +879,9 @@ def test_captured_round_matches_oracle(case):
         return gpu(d["probs"], d["root"], q, kc.clone(), None if vc is None else vc.clone(),
                    plen.clone(), kt, vt, tl)
 
-    # "batched_overlap": the target argmax on the second stream (forked and
-    # joined inside the graph)
-    ov = True if case.endswith("overlap") else None
+    # "batched_one_stream": the round without the second stream for the
+    # target argmax (the fused walk and commit)
+    ov = False if case.endswith("one_stream") else None
     eager = TreeVerifyStep.for_workload(w, DEV, overlap_argmax=ov)
     ge = fresh()
     eager._round(*ge, *extra, None)

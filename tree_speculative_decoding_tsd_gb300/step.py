@@ -66,21 +66,16 @@ class TreeVerifyStep:
         self.ws_build = workspace(tsd_tree_build_workspace_size(B, S, V, k), dev)
         self.ws_verify = workspace(tsd_verify_workspace_size(self.desc), dev)
         self.ws_walk = workspace(tsd_accept_walk_workspace_size(B, D, V), dev)
-        # The target argmax of a round reads only the logits, so it may run on
-        # a second stream beside the tree build and the attention, the walk
-        # waiting for it (fork and join by events, also inside a captured
-        # graph).  Measured on a GB300 that pays when the logits are about as
-        # large as the attention's KV and large in absolute terms (32 requests
-        # of 1-4k prefixes: step 241 -> 231 us); where the attention dominates
-        # (32k prefixes) the argmax only competes with it (+6 us), and a small
-        # step loses its launch overlap to the fork and join (+4.6 us).  None
-        # chooses by those sizes.
-        es = 2 if dtype == torch.bfloat16 else 4
-        logits_bytes = B * R * V * 4
-        kv_bytes = B * Hkv * cap * (dk + (0 if v_aliases_k else dv)) * es
-        if overlap_argmax is None:
-            overlap_argmax = logits_bytes >= (64 << 20) and logits_bytes >= kv_bytes
-        self.overlap_argmax = bool(overlap_argmax)
+        # The target argmax of a round reads only the logits, so it runs on a
+        # second stream and the walk waits for it (fork and join by events,
+        # also inside a captured graph).  It is forked after the tree build
+        # and enqueued after the attention, so the attention's CTAs go first
+        # and the argmax fills the SMs its last wave leaves idle.  Measured on
+        # a GB300 (captured step): 32k prefixes 430.7 -> 423.9 us, latent heads
+        # 2063 -> 2010 us, qwen-sized 33.4 -> 31.6 us, 32 requests of 1-4k
+        # prefixes 231.9 -> 231.3 us.  overlap_argmax=False keeps the round on
+        # one stream (the fused tsd_accept_commit).
+        self.overlap_argmax = True if overlap_argmax is None else bool(overlap_argmax)
         self.side = torch.cuda.Stream(device=dev)
         self.ev_fork = torch.cuda.Event()
         self.ev_join = torch.cuda.Event()
@@ -130,9 +125,8 @@ class TreeVerifyStep:
 
     def run(self, probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits,
             stream=None):
-        """The whole step: build -> verify -> target argmax, walk and commit
-        (asynchronous); with ``overlap_argmax`` the target argmax runs beside
-        build and verify on a second stream."""
+        """The whole step: build -> verify -> walk and commit, the target argmax
+        on a second stream beside the attention (asynchronous)."""
         self._round(probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits, None,
                     None, stream)
 
@@ -167,19 +161,19 @@ class TreeVerifyStep:
     def _round(self, probs, root_tok, q, kcache, vcache, prefix_len, ktree, vtree, logits,
                cost_d, cost_v, stream):
         main = stream if stream is not None else torch.cuda.current_stream(probs.device)
-        if self.overlap_argmax:
-            self.ev_fork.record(main)
-            self.side.wait_event(self.ev_fork)
-            tsd_target_argmax(logits, self.ws_walk, self.side)
-            self.ev_join.record(self.side)
         if cost_v is None:
             self.build(probs, root_tok, main)
         else:
             self.build_adaptive(probs, root_tok, cost_d, cost_v, main)
+        if self.overlap_argmax:
+            self.ev_fork.record(main)
         self.verify(q, kcache, vcache, prefix_len, ktree, vtree, main)
         if not self.overlap_argmax:
             self.accept_commit(logits, ktree, vtree, kcache, vcache, prefix_len, main)
             return
+        self.side.wait_event(self.ev_fork)
+        tsd_target_argmax(logits, self.ws_walk, self.side)
+        self.ev_join.record(self.side)
         main.wait_event(self.ev_join)
         t, w = self.tree, self.walk
         tsd_walk_commit(self.V, self.S, t.token, t.parent, t.mask, t.is_leaf, w.tgt,
